@@ -1,0 +1,329 @@
+"""Benchmark: batched speculative-decoding verification on GB300.
+
+Workload (the headline configuration): B=64 sequences, k=8 drafts,
+V=128256, bf16 logits, temperature 0.7, stochastic verification (accept scan,
+residual / bonus sampling).  Target logits ~ N(0, 4^2) - 1.1 ln(v+1), draft =
+target + N(0, 1^2), draft tokens drawn from the draft softmax.  Synthetic,
+seeded inputs; 279 MB of logits per step (larger than the 129 MB L2), and two
+copies alternate between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  `value` is verified rows/s, B*(k+1) per step, from CUDA
+events around K back-to-back calls (inputs resident in HBM); `e2e` repeats the
+measurement through the public call with the inputs in pinned host memory,
+the host->device copies and the device->host read of the result inside the
+timed region.  `roofline` is for the dominant kernel (the row-statistics
+pass), timed by events the library records around it on the launch stream.
+`--impl reference` times the CPU oracle on a bounded sample of the same
+workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "verified rows/s (B·(k+1)/s) and HBM GB/s vs GB300 peak, B=64 k=8 V=128256 bf16"
+B, K, V, T, SEED, GEN_SEED = 64, 8, 128256, 0.7, 1234, 103
+WORKLOAD = "C3 stochastic verification: B=64 k=8 V=128256 bf16 logits, T=0.7"
+ELEM = 2  # bf16 bytes
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        try:
+            rows = [r.split(",") for r in open(self.path).read().strip().splitlines() if r.strip()]
+            os.unlink(self.path)
+        except Exception:
+            return out
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [c.strip() for c in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if sm:
+            out.update(sm_mhz=statistics.median(sm), sm_max_mhz=max(smax), reasons=sorted(reasons),
+                       samples=len(sm))
+        return out
+
+
+def make_inputs():
+    import workloads as wl
+    return wl.c3(seed=GEN_SEED, verify_seed=SEED)
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def cpu_oracle_run(w, seconds: float = 12.0, max_reps: int = 50):
+    """Time the oracle on a bounded sample: the first 8 sequences of the workload,
+    repeated until about `seconds` of CPU work.  Returns rows/s and a description."""
+    from oracle import verify as ov
+    nb = 8
+    t = w.target[:nb]
+    d = w.draft[:nb]
+    x = w.tokens[:nb]
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        ov.verify_stochastic(t, d, x, w.dtype, w.temperature, w.seed)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or reps >= max_reps:
+            break
+    rows = reps * nb * (w.k + 1)
+    return rows / el, f"{reps} x oracle verify of sequences 0..{nb - 1} of the workload ({el:.1f} s, fp64 numpy)"
+
+
+def run_reference(args):
+    """The CPU oracle as it stands, on the machine's host cores.  A step verifies one
+    sequence of the workload (the bounded sample); the number of timed steps is
+    capped so the whole run ends within about two minutes."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from oracle import verify as ov
+    w = make_inputs()
+
+    def one(i):
+        b = i % B
+        ov.verify_stochastic(w.target[b:b + 1], w.draft[b:b + 1], w.tokens[b:b + 1], w.dtype, w.temperature, w.seed)
+
+    for i in range(min(args.warmup, 3)):
+        one(i)
+    t0 = time.perf_counter()
+    one(0)
+    per = time.perf_counter() - t0
+    steps = max(1, min(args.steps, int(120.0 / max(per, 1e-3))))
+    t_all = time.perf_counter()
+    for i in range(steps):
+        one(i)
+    el = time.perf_counter() - t_all
+    value = steps * (K + 1) / el
+    sample = f"one sequence of the workload per step ({steps} of {args.steps} requested steps timed), fp64 numpy"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": args.gpus,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B, "k": K, "V": V, "temperature": T, "input_dtype": "bf16"},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import speculative_decoding_draft_online_gb300 as sv
+
+    w = make_inputs()
+    tgt_np = w.target.view(np.int16)
+    drf_np = w.draft.view(np.int16)
+    copies = []
+    for _ in range(2):
+        copies.append((torch.from_numpy(tgt_np).to(dev).view(torch.bfloat16),
+                       torch.from_numpy(drf_np).to(dev).view(torch.bfloat16)))
+    tokens = torch.from_numpy(w.tokens).to(dev)
+    stream = torch.cuda.current_stream(dev)
+    ws = sv.workspace(B, K, V, sv.SPEC_BF16, dev)
+    out = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    n = torch.empty((B,), dtype=torch.int32, device=dev)
+
+    def step(i, events=None):
+        t, d = copies[i & 1]
+        sv.verify_ex(t, d, tokens, T, SEED, out_tokens=out, out_n=n, ws=ws, events=events)
+
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    torch.cuda.synchronize()
+    n_host = n.cpu().numpy()
+    resid_bytes = int(sum(2 * V * ELEM if nb < K else V * ELEM for nb in n_host))
+    row_bytes = B * 2 * K * V * ELEM
+    step_bytes = row_bytes + resid_bytes
+
+    # --- device-timed region: K back-to-back calls, kernel events recorded by the library
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for i in range(args.steps):
+            step(i, ev[i])
+        stop.record(stream)
+        torch.cuda.synchronize()
+    clocks = clk.summary()
+    elapsed = start.elapsed_time(stop) / 1e3
+    if world > 1:
+        tt = torch.tensor([elapsed], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        elapsed = float(tt.item())
+        torch.distributed.barrier()
+    row_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    samp_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
+    rows_per_step = B * (K + 1)
+    value = world * rows_per_step * args.steps / elapsed
+
+    # --- end to end through the public call: pinned host inputs -> device -> verify -> host result
+    h_t = torch.from_numpy(tgt_np).pin_memory()
+    h_d = torch.from_numpy(drf_np).pin_memory()
+    h_x = torch.from_numpy(w.tokens).pin_memory()
+    h_out = torch.empty((B, K + 1), dtype=torch.int32).pin_memory()
+    h_n = torch.empty((B,), dtype=torch.int32).pin_memory()
+    d_t = torch.empty(tgt_np.shape, dtype=torch.int16, device=dev)
+    d_d = torch.empty(drf_np.shape, dtype=torch.int16, device=dev)
+    d_x = torch.empty(w.tokens.shape, dtype=torch.int32, device=dev)
+
+    def e2e_step():
+        d_t.copy_(h_t, non_blocking=True)
+        d_d.copy_(h_d, non_blocking=True)
+        d_x.copy_(h_x, non_blocking=True)
+        sv.verify(d_t.view(torch.bfloat16), d_d.view(torch.bfloat16), d_x, T, SEED, out_tokens=out, out_n=n, ws=ws)
+        h_out.copy_(out, non_blocking=True)
+        h_n.copy_(n, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        e2e_step()
+    e2e_steps = max(5, min(50, args.steps // 20))
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_el = time.perf_counter() - t0
+    if world > 1:
+        tt = torch.tensor([e2e_el], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e2e_el = float(tt.item())
+    assert np.array_equal(h_n.numpy(), n_host), "e2e result differs from the device-resident run"
+    h2d = h_t.numel() * 2 + h_d.numel() * 2 + h_x.numel() * 4
+    d2h = h_out.numel() * 4 + h_n.numel() * 4
+
+    peak, peak_kind = peaks()
+    achieved = row_bytes / (row_ms / 1e3) / 1e9
+    traffic = None
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            traffic = json.load(f).get("row_pass_bytes_per_launch")
+    except Exception:
+        pass
+
+    line = None
+    if rank == 0:
+        cpu_rate, cpu_sample = cpu_oracle_run(w) if world == 1 and not args.no_cpu_baseline else (None, None)
+        line = {
+            "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "B": B, "k": K, "V": V, "temperature": T, "input_dtype": "bf16",
+                       "l2": "inputs 279 MB > 129 MB L2; two copies alternate", "parallelism": f"replicas x{world}",
+                       "step_bytes": step_bytes, "residual_bytes": resid_bytes,
+                       "step_hbm_gbs": step_bytes / (elapsed / args.steps) / 1e9,
+                       "sample_pass_ms": samp_ms, "row_pass_ms": row_ms},
+            "roofline": {"bound": "hbm", "kernel": "row_pass_kernel", "achieved": achieved, "peak": peak,
+                         "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                         "algorithmic_bytes": row_bytes},
+            "e2e": {"value": rows_per_step * e2e_steps * world / e2e_el, "unit": "rows/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+            "gpu_launches": 2 * args.steps,
+            "clocks": clocks,
+        }
+        if cpu_rate is not None:
+            line["cpu_baseline"] = {"value": cpu_rate, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                                    "sample": cpu_sample}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle CPU baseline leg")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,49 @@
+"""Compile libspecverify.so in place (nvcc, sm_103a only).
+
+    python -m speculative_decoding_draft_online_gb300.build
+
+Runs on the machine that will load the library: the x86 build host and the
+aarch64 GPU hosts each compile their own copy.
+"""
+from __future__ import annotations
+
+import os
+import subprocess
+import sys
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+LIB = os.path.join(PKG, "libspecverify.so")
+
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-shared", "-cudart", "shared",
+              "-Xptxas", "-v", "--resource-usage"]
+
+
+def nvcc() -> str:
+    for cand in (os.environ.get("NVCC"), "/usr/local/cuda/bin/nvcc", "nvcc"):
+        if cand and (os.path.isabs(cand) and os.path.exists(cand) or not os.path.isabs(cand)):
+            return cand
+    return "nvcc"
+
+
+def sources():
+    return [os.path.join(CSRC, "spec_verify.cu")]
+
+
+def build(verbose: bool = False, out: str = LIB) -> str:
+    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-I", INCLUDE, "-I", CSRC, *sources(), "-o", out]
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    if res.returncode != 0:
+        sys.stderr.write(res.stdout + res.stderr)
+        raise RuntimeError(f"nvcc failed ({res.returncode}): {' '.join(cmd)}")
+    if verbose:
+        sys.stderr.write(res.stderr)
+    return out
+
+
+if __name__ == "__main__":
+    build(verbose=True)
+    print(LIB)

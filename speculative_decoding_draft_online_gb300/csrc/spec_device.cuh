@@ -1,0 +1,178 @@
+// Device helpers for the verification kernels (sm_103a).
+//
+// Nothing here is shared with the CPU oracle; the Philox block function below
+// is written from its published definition (Salmon, Moraes, Dror, Shaw,
+// "Parallel random numbers: as easy as 1, 2, 3", SC'11).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <math_constants.h>
+#include <stdint.h>
+
+namespace sv {
+
+constexpr int kThreads = 256;          // threads per CTA of every kernel
+constexpr int kWarps = kThreads / 32;
+constexpr int kTile = 2048;            // row pass: partition granularity, elements
+constexpr int kUnroll = 4;             // row pass: 16-byte vectors in flight per thread
+constexpr int kSampleTile = 4096;      // sampling pass: elements per CTA
+
+// ---------------------------------------------------------------- Philox ---
+// Ten rounds of Philox4x32: counter words 0 and 2 are multiplied by two fixed
+// odd constants; the high halves are xored with the other counter words and
+// the key; the key takes a Weyl increment between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 key) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r) {
+      key.x += 0x9E3779B9u;
+      key.y += 0xBB67AE85u;
+    }
+    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(hi1 ^ c.y ^ key.x, lo1, hi0 ^ c.w ^ key.y, lo0);
+  }
+  return c;
+}
+
+__device__ __forceinline__ uint2 philox_key(uint64_t seed) {
+  return make_uint2((uint32_t)seed, (uint32_t)(seed >> 32));
+}
+
+// U(w) = ((w >> 9) + 0.5) * 2^-23: every step is exact in fp32.
+__device__ __forceinline__ float uniform_of(uint32_t w) {
+  return ((float)(w >> 9) + 0.5f) * 0x1p-23f;
+}
+
+// Standard Gumbel noise from a uniform, with the accurate logf (the inner
+// logarithm of a uniform near 1 must keep its relative accuracy).
+__device__ __forceinline__ float gumbel_of(float u) { return -logf(-logf(u)); }
+
+// Uniform deciding draft position i of sequence b.
+__device__ __forceinline__ float accept_uniform(uint2 key, int b, int i) {
+  return uniform_of(philox4x32_10(make_uint4(0u, (uint32_t)i, (uint32_t)b, 0u), key).x);
+}
+
+// The four Gumbel uniforms of ids 4g .. 4g+3 on row j of sequence b.
+__device__ __forceinline__ uint4 gumbel_words(uint2 key, int b, int j, uint32_t g) {
+  return philox4x32_10(make_uint4(g, (uint32_t)j, (uint32_t)b, 1u), key);
+}
+
+// ------------------------------------------------------------ arithmetic ---
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// max that returns NaN if either operand is NaN.
+__device__ __forceinline__ float nanmax(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+
+// Packed bf16x2 max that propagates NaN.
+__device__ __forceinline__ uint32_t bf16x2_nanmax(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// bf16 -> fp32 is exact: the 16 bits become the top half of the fp32 word.
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16_at(const uint16_t* p, size_t i) {
+  return __uint_as_float(((uint32_t)__ldg(p + i)) << 16);
+}
+
+// Streaming 16-byte load: read once, do not keep in L1.
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// ---------------------------------------------------- (value, index) order ---
+// a beats b: larger value, then lower index.  Index INT_MAX stands for "none".
+__device__ __forceinline__ bool beats(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+// -------------------------------------------------------- block reductions ---
+// All threads of the CTA must call these; results are returned to every thread.
+struct BlockScratch {
+  float f[kWarps];
+  float g[kWarps];
+  int i[kWarps];
+  int flag;
+};
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ void warp_argmax(float& v, int& i) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+    if (beats(ov, oi, v, i)) { v = ov; i = oi; }
+  }
+}
+
+// Scale of a partial sum kept relative to max m when the common max is M >= m.
+__device__ __forceinline__ float rescale(float s, float m, float M, float c) {
+  return (m == M) ? s : s * ex2_approx((m - M) * c);
+}
+
+// Combine per-thread (max, sum of exp2((x - max) c)) pairs over the CTA.
+__device__ __forceinline__ void block_lse(float& m, float& s, float c, BlockScratch& sh) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  float M = warp_max(m);
+  s = warp_sum(rescale(s, m, M, c));
+  if (lane == 0) { sh.f[w] = M; sh.g[w] = s; }
+  __syncthreads();
+  float bm = (lane < kWarps) ? sh.f[lane] : -CUDART_INF_F;
+  float bs = (lane < kWarps) ? sh.g[lane] : 0.f;
+  const float BM = warp_max(bm);
+  bs = warp_sum(rescale(bs, bm, BM, c));
+  __syncthreads();
+  m = BM;
+  s = bs;
+}
+
+__device__ __forceinline__ void block_argmax(float& v, int& i, BlockScratch& sh) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  warp_argmax(v, i);
+  if (lane == 0) { sh.f[w] = v; sh.i[w] = i; }
+  __syncthreads();
+  float bv = (lane < kWarps) ? sh.f[lane] : -CUDART_INF_F;
+  int bi = (lane < kWarps) ? sh.i[lane] : 0x7fffffff;
+  warp_argmax(bv, bi);
+  __syncthreads();
+  v = bv;
+  i = bi;
+}
+
+__device__ __forceinline__ int block_or(int x, BlockScratch& sh) {
+  if (threadIdx.x == 0) sh.flag = 0;
+  __syncthreads();
+  if (x) atomicOr(&sh.flag, 1);
+  __syncthreads();
+  const int r = sh.flag;
+  __syncthreads();
+  return r;
+}
+
+}  // namespace sv

@@ -1,0 +1,307 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Covers the five workloads at full size, the stochastic i.i.d.-acceptance
+construction, and the edge cases of the method (k at warp boundaries, ragged
+and unaligned vocabularies, masked vocabulary, ties, huge logits, bad tokens,
+non-finite logits, workspace reuse, streams).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+from oracle import theory
+from oracle import verify as ov
+from tests.gpu_parity import Tally, compare_probs, compare_stochastic, to_device, tokens_to_device
+
+pytestmark = pytest.mark.gpu
+
+TALLY = Tally()
+
+
+@pytest.fixture(scope="module")
+def sv():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    import speculative_decoding_draft_online_gb300 as sv
+    return sv
+
+
+def run_stochastic(sv, w, seed=None, **kw):
+    seed = w.seed if seed is None else seed
+    t = to_device(w.target, w.dtype)
+    d = to_device(w.draft, w.dtype)
+    x = tokens_to_device(w.tokens)
+    out, n, aux = sv.verify_ex(t, d, x, w.temperature, seed, aux=True, **kw)
+    torch.cuda.synchronize()
+    ref = ov.verify_stochastic(w.target, w.draft, w.tokens, w.dtype, w.temperature, seed)
+    tally = compare_stochastic(ref, out.cpu().numpy(), n.cpu().numpy(), aux["status"].cpu().numpy(), w.k)
+    compare_probs(ref, aux, w.k)
+    TALLY.add(tally)
+    return ref, out.cpu().numpy(), n.cpu().numpy()
+
+
+def run_greedy(sv, w):
+    t = to_device(w.target, w.dtype)
+    x = tokens_to_device(w.tokens)
+    out, n, aux = sv.verify_ex(t, None, x, 0.0, 0, aux=True)
+    torch.cuda.synchronize()
+    ref = ov.verify_greedy(w.target, w.tokens, w.dtype)
+    np.testing.assert_array_equal(aux["status"].cpu().numpy(), ref.status)
+    ok = ref.status == 0
+    np.testing.assert_array_equal(out.cpu().numpy()[ok], ref.out_tokens[ok])
+    np.testing.assert_array_equal(n.cpu().numpy()[ok], ref.n_accepted[ok])
+    assert np.all(n.cpu().numpy()[~ok] == -1)
+    return ref, out.cpu().numpy(), n.cpu().numpy()
+
+
+# ------------------------------------------------------------- workloads ---
+
+def test_c1_tiny_stochastic_and_greedy(sv):
+    for vs in range(40):
+        w = wl.c1_tiny(verify_seed=1234 + vs)
+        run_stochastic(sv, w)
+    run_greedy(sv, wl.c1_tiny())
+
+
+def test_c2_stochastic_many_seeds(sv):
+    w = wl.c2()
+    for vs in range(50):
+        run_stochastic(sv, w, seed=1234 + 7919 * vs)
+
+
+def test_c3_headline_stochastic_and_greedy(sv):
+    """B=64, k=8, V=128256, bf16, T=0.7: the bench's workload, full size."""
+    w = wl.c3()
+    for vs in range(3):
+        run_stochastic(sv, w, seed=1234 + vs)
+    run_greedy(sv, w)
+
+
+@pytest.mark.parametrize("a", [0.6, 0.8])
+def test_c4_phrase_drafts_greedy(sv, a):
+    """B=16, k=16, V=64000: bit-exact, and the committed count follows (1-a^17)/(1-a)."""
+    m = []
+    for s in range(12):
+        w = wl.c4(a, seed=104 + 1000 * s)
+        _, _, n = run_greedy(sv, w)
+        m.append(n + 1)
+    m = np.concatenate(m)
+    pmf = theory.committed_pmf(a, 16)
+    mu = theory.expected_committed(a, 16)
+    sd = math.sqrt((np.arange(18) ** 2 * pmf).sum() - mu ** 2)
+    assert abs(m.mean() - mu) < 4 * sd / math.sqrt(m.size)
+
+
+def test_c5_tree(sv):
+    w = wl.c5()
+    t = to_device(w.target, w.dtype)
+    out, n, leaf, status = sv.verify_tree(t, tokens_to_device(w.tokens), tokens_to_device(w.parents))
+    torch.cuda.synchronize()
+    ref = ov.verify_tree(w.target, w.tokens, w.parents, w.dtype)
+    np.testing.assert_array_equal(status.cpu().numpy(), ref.status)
+    np.testing.assert_array_equal(out.cpu().numpy(), ref.out_tokens)
+    np.testing.assert_array_equal(n.cpu().numpy(), ref.n_accepted)
+    np.testing.assert_array_equal(leaf.cpu().numpy(), ref.leaf)
+
+
+@pytest.mark.parametrize("a", [0.6, 0.8])
+def test_iid_acceptance_construction(sv, a):
+    w = wl.iid_acceptance(256, 4, 64, a, seed=int(a * 10))
+    ref, out, n = run_stochastic(sv, w)
+    assert abs((n + 1).mean() - theory.expected_committed(a, 4)) < 0.25
+
+
+# ------------------------------------------------------------- edge cases ---
+
+@pytest.mark.parametrize("k", [1, 31, 32, 33, 64])
+def test_k_around_warp_boundaries(sv, k):
+    w = wl.gaussian_pair(3, k, 1000, wl.BF16, 1.0, seed=k, sigma_t=1.0, sigma_d=0.3)
+    run_stochastic(sv, w)
+    w = wl.c4(0.9, seed=k, B=3, k=k, V=1000)
+    run_greedy(sv, w)
+
+
+@pytest.mark.parametrize("V", [1, 2, 7, 1001, 2047, 2048, 2049, 4097, 8193])
+@pytest.mark.parametrize("dtype", [wl.BF16, wl.FP32])
+def test_ragged_vocabularies(sv, V, dtype):
+    w = wl.gaussian_pair(5, 3, V, dtype, 0.9, seed=V, sigma_t=2.0, sigma_d=1.0)
+    run_stochastic(sv, w)
+    run_greedy(sv, w)
+
+
+def test_unaligned_base_pointer(sv):
+    """Rows that start off a 16-byte boundary take the scalar head path."""
+    w = wl.gaussian_pair(4, 3, 3001, wl.BF16, 1.0, seed=9, sigma_t=3.0, sigma_d=1.0)
+    for off in (1, 3):
+        tb = torch.empty(w.target.size + off, dtype=torch.int16, device="cuda")
+        tb[off:] = torch.from_numpy(w.target.view(np.int16).ravel()).cuda()
+        db = torch.empty(w.draft.size + off, dtype=torch.int16, device="cuda")
+        db[off:] = torch.from_numpy(w.draft.view(np.int16).ravel()).cuda()
+        t = tb[off:].view(torch.bfloat16).view(w.target.shape)
+        d = db[off:].view(torch.bfloat16).view(w.draft.shape)
+        assert t.data_ptr() % 16 != 0
+        out, n, aux = sv.verify_ex(t, d, tokens_to_device(w.tokens), 1.0, 77, aux=True)
+        torch.cuda.synchronize()
+        ref = ov.verify_stochastic(w.target, w.draft, w.tokens, w.dtype, 1.0, 77)
+        TALLY.add(compare_stochastic(ref, out.cpu().numpy(), n.cpu().numpy(), aux["status"].cpu().numpy(), w.k))
+        compare_probs(ref, aux, w.k)
+        g, gn = sv.verify(t, None, tokens_to_device(w.tokens), 0.0)
+        gref = ov.verify_greedy(w.target, w.tokens, w.dtype)
+        np.testing.assert_array_equal(g.cpu().numpy(), gref.out_tokens)
+
+
+def test_single_sequence_and_temperatures(sv):
+    for T in (0.05, 0.3, 1.0, 4.0, 25.0):
+        w = wl.gaussian_pair(1, 5, 5000, wl.FP32, T, seed=int(T * 100), sigma_t=2.0, sigma_d=0.7)
+        run_stochastic(sv, w)
+
+
+def test_masked_vocabulary(sv):
+    """-inf logits (masked ids): p_v = 0 there; masked draft tokens are rejected."""
+    rng = np.random.default_rng(3)
+    w = wl.gaussian_pair(8, 4, 3000, wl.FP32, 1.0, seed=31, sigma_t=3.0, sigma_d=1.0)
+    t = w.target.copy()
+    d = w.draft.copy()
+    t[rng.random(t.shape) < 0.3] = -np.inf
+    d[rng.random(d.shape) < 0.3] = -np.inf
+    t[0, 1, w.tokens[0, 1]] = -np.inf          # p(x) = 0: must reject
+    d[1, 0, w.tokens[1, 0]] = -np.inf          # q(x) = 0: q <= p, must accept
+    w.target, w.draft = t, d
+    ref, out, n = run_stochastic(sv, w)
+    assert n[0] <= 1
+
+
+def test_greedy_ties_take_the_lowest_index(sv):
+    rng = np.random.default_rng(5)
+    for dtype in (wl.BF16, wl.FP32):
+        x = rng.integers(-2, 3, size=(6, 9, 5000)).astype(np.float32)   # massive ties
+        x[2, 3, :] = 1.5                                                   # all-equal row
+        x[3, 4, :] = -np.inf                                               # all -inf row
+        tgt = wl.store(x, dtype)
+        arg = ov.row_argmax(ov.decode_logits(tgt, dtype))
+        tokens = np.where(rng.random((6, 8)) < 0.8, arg[:, :8], 1).astype(np.int32)
+        w = wl.Workload("ties", "greedy", 6, 8, 5000, dtype, 0.0, tgt, None, tokens)
+        ref, out, n = run_greedy(sv, w)
+        assert ref.argmax[2, 3] == 0 and ref.argmax[3, 4] == 0
+
+
+def test_huge_logits(sv):
+    w = wl.gaussian_pair(4, 3, 2000, wl.FP32, 1.0, seed=12, sigma_t=3.0, sigma_d=1.0)
+    w.target[0, 0, 5] = 3e4
+    w.draft[1, 1, 7] = 3e4
+    w.target[2, :, 9] = -3e4
+    run_stochastic(sv, w)
+
+
+def test_bad_tokens_and_nonfinite_set_status(sv):
+    w = wl.gaussian_pair(5, 3, 700, wl.FP32, 1.0, seed=13, sigma_t=2.0, sigma_d=1.0)
+    w.tokens[1, 2] = 700                       # out of range
+    w.tokens[2, 0] = -1
+    w.target[3, 1, 10] = np.nan
+    w.draft[4, 2, 11] = np.inf
+    ref, out, n = run_stochastic(sv, w)
+    assert list(ref.status) == [0, -3, -3, -4, -4]
+    g = wl.Workload("g", "greedy", 5, 3, 700, wl.FP32, 0.0, w.target, None, w.tokens)
+    run_greedy(sv, g)
+
+
+def test_all_masked_row_is_nonfinite(sv):
+    w = wl.gaussian_pair(3, 2, 300, wl.FP32, 1.0, seed=14, sigma_t=2.0, sigma_d=1.0)
+    w.draft[1, 1, :] = -np.inf
+    ref, _, _ = run_stochastic(sv, w)
+    assert ref.status[1] == -4
+
+
+def test_workspace_reuse_and_determinism(sv):
+    """Counters return to zero: one workspace serves different shapes and modes in turn."""
+    ws = sv.workspace(64, 16, 200000, sv.SPEC_BF16, "cuda")
+    ws2 = torch.zeros_like(ws)
+    w1 = wl.gaussian_pair(6, 5, 3333, wl.BF16, 0.8, seed=1, sigma_t=3.0, sigma_d=1.0)
+    w2 = wl.c4(0.7, seed=2, B=5, k=9, V=4000)
+    t1, d1, x1 = to_device(w1.target, w1.dtype), to_device(w1.draft, w1.dtype), tokens_to_device(w1.tokens)
+    t2, x2 = to_device(w2.target, w2.dtype), tokens_to_device(w2.tokens)
+    first = sv.verify(t1, d1, x1, 0.8, 99, ws=ws)
+    for _ in range(3):
+        again = sv.verify(t1, d1, x1, 0.8, 99, ws=ws)
+        g = sv.verify(t2, None, x2, 0.0, ws=ws)
+        fresh = sv.verify(t1, d1, x1, 0.8, 99, ws=ws2)
+        torch.cuda.synchronize()
+        assert torch.equal(first[0], again[0]) and torch.equal(first[1], again[1])
+        assert torch.equal(first[0], fresh[0])
+        gref = ov.verify_greedy(w2.target, w2.tokens, w2.dtype)
+        np.testing.assert_array_equal(g[0].cpu().numpy(), gref.out_tokens)
+
+
+def test_side_stream(sv):
+    w = wl.gaussian_pair(4, 4, 5000, wl.BF16, 1.0, seed=21, sigma_t=3.0, sigma_d=1.0)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        t, d, x = to_device(w.target, w.dtype), to_device(w.draft, w.dtype), tokens_to_device(w.tokens)
+        out, n = sv.verify(t, d, x, 1.0, 5, stream=s)
+    s.synchronize()
+    ref = ov.verify_stochastic(w.target, w.draft, w.tokens, w.dtype, 1.0, 5)
+    TALLY.add(compare_stochastic(ref, out.cpu().numpy(), n.cpu().numpy(), np.zeros(4, np.int32), w.k))
+
+
+@pytest.mark.parametrize("shape", ["chain", "wide", "random"])
+def test_tree_shapes(sv, shape):
+    rng = np.random.default_rng(len(shape))
+    if shape == "chain":
+        par = np.arange(-1, 11, dtype=np.int32)
+    elif shape == "wide":
+        par = np.full(40, -1, dtype=np.int32)
+    else:
+        par = np.array([-1] + [int(rng.integers(-1, m)) for m in range(1, 60)], dtype=np.int32)
+    w = wl.c5(seed=7, B=6, V=3001, p_match=0.8, dtype=wl.FP32, parents=par)
+    out, n, leaf, status = sv.verify_tree(to_device(w.target, w.dtype), tokens_to_device(w.tokens),
+                                          tokens_to_device(w.parents))
+    ref = ov.verify_tree(w.target, w.tokens, w.parents, w.dtype)
+    np.testing.assert_array_equal(out.cpu().numpy(), ref.out_tokens)
+    np.testing.assert_array_equal(n.cpu().numpy(), ref.n_accepted)
+    np.testing.assert_array_equal(leaf.cpu().numpy(), ref.leaf)
+    if shape == "chain":
+        g = ov.verify_greedy(w.target, w.tokens, w.dtype)      # a chain of 12 nodes is k = 12
+        np.testing.assert_array_equal(out.cpu().numpy(), g.out_tokens)
+
+
+def test_tree_bad_parent(sv):
+    w = wl.c5(seed=8, B=3, V=500, dtype=wl.FP32)
+    w.parents[1, 5] = 9                        # a parent after its child
+    out, n, leaf, status = sv.verify_tree(to_device(w.target, w.dtype), tokens_to_device(w.tokens),
+                                          tokens_to_device(w.parents))
+    ref = ov.verify_tree(w.target, w.tokens, w.parents, w.dtype)
+    np.testing.assert_array_equal(status.cpu().numpy(), ref.status)
+    assert ref.status[1] == -3 and n.cpu().numpy()[1] == -1
+
+
+def test_random_stream_matches_oracle(sv):
+    from oracle import philox
+    for seed, b, j in ((1234, 0, 0), (2 ** 40 + 5, 63, 8), (7, 3, 17)):
+        u, g, a = sv.random_stream(seed, b, j, 10007)
+        torch.cuda.synchronize()
+        ru = philox.gumbel_uniforms(seed, b, j, 10007)
+        np.testing.assert_array_equal(u.cpu().numpy().astype(np.float64), ru)
+        rg = philox.gumbel(ru)
+        np.testing.assert_allclose(g.cpu().numpy(), rg, rtol=2e-6, atol=2e-6)
+        assert float(a.cpu()[0]) == philox.accept_uniform(seed, b, j)
+
+
+def test_host_side_argument_errors(sv):
+    t = torch.zeros((2, 3, 10), dtype=torch.bfloat16, device="cuda")
+    x = torch.zeros((2, 2), dtype=torch.int32, device="cuda")
+    with pytest.raises(sv.SpecError):
+        sv.verify(t, t[:, :2].contiguous(), x, -1.0)
+    with pytest.raises(sv.SpecError):
+        sv.verify(t, t[:, :2].contiguous(), x, float("nan"))
+    with pytest.raises(sv.SpecError):
+        sv.verify_tree(t, x, x, temperature=0.5)
+
+
+def test_margin_rows_under_one_in_ten_thousand():
+    """Positions excused by the margin rule stay under 0.01 % of those compared."""
+    if TALLY.rows < 10_000:
+        pytest.skip(f"only {TALLY.rows} positions compared in this run (a subset was selected)")
+    assert TALLY.margin_rows < 1e-4 * TALLY.rows, TALLY
