@@ -40,7 +40,9 @@
  *
  * Workspace: a caller-owned device buffer of spec_workspace_size() bytes.  It
  * must be zero-filled once before its first use (spec_workspace_init or any
- * memset); every call that returns SPEC_OK leaves it zero-filled again.  Two
+ * memset).  A call returns the completion counters inside it to zero; when a
+ * workspace is used with sizes other than those of its previous call, the
+ * library clears it first (one cudaMemsetAsync on the call's stream).  Two
  * calls that may overlap in time must not share a workspace.
  *
  * Errors: argument errors are detected on the host and returned before any
@@ -121,6 +123,9 @@ typedef struct spec_verify_aux {
   int32_t* status;     /* device [B]: SPEC_OK or the sequence's device-detected error       */
   void* events[4];     /* cudaEvent_t recorded on cuda_stream: before / after the row pass, */
                        /*   before / after the sampling pass (stochastic) -- for timing     */
+  uint32_t sequence_offset; /* global index of sequence 0 in the Philox counters: a batch  */
+                       /*   split across devices draws the same numbers as the whole batch  */
+                       /*   when each shard passes the index of its first sequence          */
 } spec_verify_aux;
 
 /* spec_verify plus the auxiliary outputs in `aux` (which may be NULL). */

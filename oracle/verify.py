@@ -161,10 +161,12 @@ class StochasticResult:
     empty_residual: np.ndarray  # [B] bool
 
 
-def verify_stochastic(target, draft, tokens, dtype: str, temperature: float, seed: int) -> StochasticResult:
+def verify_stochastic(target, draft, tokens, dtype: str, temperature: float, seed: int,
+                      seq_offset: int = 0) -> StochasticResult:
     """Stochastic verification of B sequences (oracle).
 
-    target [B][k+1][V], draft [B][k][V] stored logits; tokens [B][k].
+    target [B][k+1][V], draft [B][k][V] stored logits; tokens [B][k].  Sequence b
+    draws the randomness of global sequence index seq_offset + b.
     """
     t = decode_logits(target, dtype)
     d = decode_logits(draft, dtype)
@@ -194,15 +196,16 @@ def verify_stochastic(target, draft, tokens, dtype: str, temperature: float, see
             logq, lse_d[b] = log_softmax(d[b], temperature)
         p_d[b] = np.exp(logp[np.arange(k), tokens[b]])
         q_d[b] = np.exp(logq[np.arange(k), tokens[b]])
-        seq, n = verify_sequence(logp, logq, tokens[b], _philox_accept(seed, b),
-                                 _gumbel_draw(seed, b, trace))
+        gb = seq_offset + b
+        seq, n = verify_sequence(logp, logq, tokens[b], _philox_accept(seed, gb),
+                                 _gumbel_draw(seed, gb, trace))
         if n == k and _bad_rows(t[b, k:k + 1]):
             status[b] = STATUS_NONFINITE
             continue
         out[b, :len(seq)] = seq
         n_acc[b] = n
         empty[b] = trace.empty_residual
-        margins[b] = position_margins(seed, b, p_d[b], q_d[b], n, k, trace.draw_gap)
+        margins[b] = position_margins(seed, gb, p_d[b], q_d[b], n, k, trace.draw_gap)
     return StochasticResult(out, n_acc, p_d, q_d, lse_t, lse_d, status, margins, empty)
 
 

@@ -32,13 +32,14 @@ class SpecError(RuntimeError):
 
 class _Aux(ctypes.Structure):
     _fields_ = [("p_draft", ctypes.c_void_p), ("q_draft", ctypes.c_void_p), ("lse", ctypes.c_void_p),
-                ("status", ctypes.c_void_p), ("events", ctypes.c_void_p * 4)]
+                ("status", ctypes.c_void_p), ("events", ctypes.c_void_p * 4),
+                ("sequence_offset", ctypes.c_uint32)]
 
 
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"{LIB_PATH} is missing: build it with "
-                          "`python -m speculative_decoding_draft_online_gb300.build`")
+                          "`python __graft_entry__.py build`")
     L = ctypes.CDLL(LIB_PATH)
     vp, i32, u64, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64, ctypes.c_float, ctypes.c_size_t
     L.spec_workspace_size.argtypes = [i32, i32, i32, i32]
@@ -121,13 +122,14 @@ def _check(t: torch.Tensor, name: str, shape, dtype=None):
 
 def verify_ex(target: torch.Tensor, draft: Optional[torch.Tensor], tokens: torch.Tensor, temperature: float,
               seed: int = 0, *, out_tokens=None, out_n=None, ws=None, stream=None, aux: bool = False,
-              events=None):
+              events=None, sequence_offset: int = 0):
     """spec_verify_ex on torch tensors.
 
     target [B][k+1][V] and draft [B][k][V] (bf16 or fp32, same dtype), tokens
     [B][k] int32.  temperature == 0 selects greedy verification (draft may be
     None).  Returns (out_tokens [B][k+1] int32, n_accepted [B] int32) and, with
-    aux=True, a dict of p_draft, q_draft, lse and status.
+    aux=True, a dict of p_draft, q_draft, lse and status.  sequence_offset is
+    the global index of sequence 0 when the batch is a shard of a larger one.
     """
     B, k1, V = target.shape
     k = k1 - 1
@@ -147,8 +149,9 @@ def verify_ex(target: torch.Tensor, draft: Optional[torch.Tensor], tokens: torch
         ws = workspace(B, k, V, code, dev, stream)
     extra = {}
     a = None
-    if aux or events is not None:
+    if aux or events is not None or sequence_offset:
         a = _Aux()
+        a.sequence_offset = int(sequence_offset)
         if aux:
             extra = dict(p_draft=torch.zeros((B, k), dtype=torch.float32, device=dev),
                          q_draft=torch.zeros((B, k), dtype=torch.float32, device=dev),

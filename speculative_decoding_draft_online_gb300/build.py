@@ -1,6 +1,6 @@
 """Compile libspecverify.so in place (nvcc, sm_103a only).
 
-    python -m speculative_decoding_draft_online_gb300.build
+    python speculative_decoding_draft_online_gb300/build.py   (or: python __graft_entry__.py build)
 
 Runs on the machine that will load the library: the x86 build host and the
 aarch64 GPU hosts each compile their own copy.

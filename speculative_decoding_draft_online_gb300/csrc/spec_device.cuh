@@ -49,13 +49,13 @@ __device__ __forceinline__ float uniform_of(uint32_t w) {
 __device__ __forceinline__ float gumbel_of(float u) { return -logf(-logf(u)); }
 
 // Uniform deciding draft position i of sequence b.
-__device__ __forceinline__ float accept_uniform(uint2 key, int b, int i) {
-  return uniform_of(philox4x32_10(make_uint4(0u, (uint32_t)i, (uint32_t)b, 0u), key).x);
+__device__ __forceinline__ float accept_uniform(uint2 key, uint32_t b, int i) {
+  return uniform_of(philox4x32_10(make_uint4(0u, (uint32_t)i, b, 0u), key).x);
 }
 
 // The four Gumbel uniforms of ids 4g .. 4g+3 on row j of sequence b.
-__device__ __forceinline__ uint4 gumbel_words(uint2 key, int b, int j, uint32_t g) {
-  return philox4x32_10(make_uint4(g, (uint32_t)j, (uint32_t)b, 1u), key);
+__device__ __forceinline__ uint4 gumbel_words(uint2 key, uint32_t b, int j, uint32_t g) {
+  return philox4x32_10(make_uint4(g, (uint32_t)j, b, 1u), key);
 }
 
 // ------------------------------------------------------------ arithmetic ---

@@ -41,6 +41,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <unordered_map>
 
 #include "spec_device.cuh"
 #include "spec_verify.h"
@@ -89,6 +90,7 @@ struct Params {
   float invT;                  // 1 / T (stochastic)
   float c;                     // log2(e) / T (stochastic)
   uint2 key;
+  uint32_t b0;                 // global index of sequence 0 (Philox counter word 2)
   int32_t* out_tokens;
   int32_t* out_n;
   int32_t* out_leaf;
@@ -310,7 +312,7 @@ __device__ void accept_scan(const Params& P, int b) {
         const float xd = load_elem<T>((const T*)P.draft, ((size_t)b * k + i) * P.V + x);
         const float lp = (xt - rt.m) * P.invT - rt.lnS;   // ln p_i(x_i)
         const float lq = (xd - rd.m) * P.invT - rd.lnS;   // ln q_i(x_i)
-        const float u = accept_uniform(P.key, b, i);
+        const float u = accept_uniform(P.key, P.b0 + (uint32_t)b, i);
         acc = (lq <= lp) || (u < expf(lp - lq));
         if (P.p_draft) P.p_draft[(size_t)b * k + i] = expf(lp);
         if (P.q_draft) P.q_draft[(size_t)b * k + i] = expf(lq);
@@ -549,7 +551,7 @@ __global__ void __launch_bounds__(kThreads) sample_pass_kernel(const Params P) {
       const T* trow = (const T*)P.target + ((size_t)b * (k + 1) + n) * P.V;
       const T* drow = (const T*)P.draft + ((size_t)b * k + n) * P.V;
       for (int g = (v0 >> 2) + threadIdx.x; 4 * g < v1; g += kThreads) {
-        const uint4 w = gumbel_words(P.key, b, n, (uint32_t)g);
+        const uint4 w = gumbel_words(P.key, P.b0 + (uint32_t)b, n, (uint32_t)g);
         const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -567,7 +569,7 @@ __global__ void __launch_bounds__(kThreads) sample_pass_kernel(const Params P) {
       // bonus: argmax of x/T + Gumbel over target row k
       const T* trow = (const T*)P.target + ((size_t)b * (k + 1) + k) * P.V;
       for (int g = (v0 >> 2) + threadIdx.x; 4 * g < v1; g += kThreads) {
-        const uint4 w = gumbel_words(P.key, b, k, (uint32_t)g);
+        const uint4 w = gumbel_words(P.key, P.b0 + (uint32_t)b, k, (uint32_t)g);
         const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -612,7 +614,7 @@ __global__ void __launch_bounds__(kThreads) sample_pass_kernel(const Params P) {
     const T* trow = (const T*)P.target + ((size_t)b * (k + 1) + n) * P.V;
     best = -CUDART_INF_F;
     for (int g = threadIdx.x; 4 * g < P.V; g += kThreads) {
-      const uint4 w = gumbel_words(P.key, b, n, (uint32_t)g);
+      const uint4 w = gumbel_words(P.key, P.b0 + (uint32_t)b, n, (uint32_t)g);
       const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
       for (int e = 0; e < 4 && 4 * g + e < P.V; ++e) {
         const int v = 4 * g + e;
@@ -704,6 +706,28 @@ static int resident_ctas(const void* fn) {
 
 static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// The completion counters sit at layout-dependent offsets, and a call returns
+// only them to zero.  A workspace used with new sizes is therefore cleared
+// first; the library remembers the sizes each workspace last served.
+static int prepare_workspace(void* ws, const Layout& L, int B, int k, int V, cudaStream_t stream) {
+  static std::mutex mu;
+  static std::unordered_map<uintptr_t, uint64_t> last;
+  const uint64_t sig = ((uint64_t)(uint32_t)V << 32) ^ ((uint64_t)(uint32_t)B << 12) ^ (uint64_t)(uint32_t)k ^
+                       ((uint64_t)(uint32_t)k << 44);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = last.find(reinterpret_cast<uintptr_t>(ws));
+    if (it != last.end() && it->second == sig) return SPEC_OK;
+    last[reinterpret_cast<uintptr_t>(ws)] = sig;
+  }
+  if (cudaMemsetAsync(ws, 0, L.total, stream) != cudaSuccess) {
+    std::lock_guard<std::mutex> lock(mu);
+    last.erase(reinterpret_cast<uintptr_t>(ws));
+    return SPEC_ERR_CUDA;
+  }
+  return SPEC_OK;
+}
+
 template <typename T, int kMode>
 static int launch_row_pass(const Params& P, cudaStream_t stream) {
   const void* fn = reinterpret_cast<const void*>(&row_pass_kernel<T, kMode>);
@@ -794,8 +818,10 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, const in
     P.p_draft = aux->p_draft;
     P.q_draft = aux->q_draft;
     P.lse = aux->lse;
+    P.b0 = aux->sequence_offset;
   }
   cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+  if ((rc = prepare_workspace(workspace, L, B, k, V, stream)) != SPEC_OK) return rc;
   if (greedy) {
     P.rows_per_seq = k + 1;
     P.R = (long long)B * (k + 1);
@@ -855,6 +881,8 @@ int spec_verify_tree(const void* target_logits, const int32_t* node_tokens, cons
   P.status = status;
   P.ws = bind(workspace, L);
   cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+  const int prc = prepare_workspace(workspace, L, B, N, V, stream);
+  if (prc != SPEC_OK) return prc;
   return dtype == SPEC_BF16 ? launch_row_pass<uint16_t, kTree>(P, stream) : launch_row_pass<float, kTree>(P, stream);
 }
 

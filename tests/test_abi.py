@@ -1,0 +1,87 @@
+"""The C ABI library loads, exports every function include/*.h declares, and
+rejects bad arguments on the host (no GPU needed: nothing here launches)."""
+import ctypes
+import glob
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+LIB = os.path.join(ROOT, "speculative_decoding_draft_online_gb300", "libspecverify.so")
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(spec_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(LIB):
+        import __graft_entry__
+        __graft_entry__.build()
+    return ctypes.CDLL(LIB)
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for want in ("spec_verify", "spec_verify_ex", "spec_verify_tree", "spec_workspace_size", "spec_workspace_init",
+                 "spec_random", "spec_strerror", "spec_abi_version"):
+        assert want in names, names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", LIB], capture_output=True, text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    missing = declared_functions() - exported
+    assert not missing, missing
+    for name in declared_functions():
+        getattr(lib, name)
+
+
+def test_workspace_size(lib):
+    lib.spec_workspace_size.restype = ctypes.c_size_t
+    ws = lib.spec_workspace_size
+    assert ws(64, 8, 128256, 0) > 0
+    assert ws(0, 8, 128256, 0) == 0 and ws(1, 0, 10, 0) == 0 and ws(1, 1, 0, 0) == 0 and ws(1, 1, 10, 7) == 0
+    assert ws(64, 8, 128256, 0) >= 64 * 16 * ((128256 + 2047) // 2048) * 8
+    assert ws(64, 8, 128256, 0) % 256 == 0
+
+
+def test_host_side_errors_return_before_any_launch(lib):
+    vp = ctypes.c_void_p
+    f = lib.spec_verify
+    f.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float,
+                  ctypes.c_uint64, vp, vp, vp, ctypes.c_size_t, vp]
+    fake = vp(0x10000)                                  # never dereferenced: every call fails on the host
+    ARG, ALIGN, UNSUP, WS = -1, -2, -5, -8
+    assert f(None, fake, fake, 1, 1, 10, 0, 1.0, 0, fake, fake, fake, 1 << 20, None) == ARG       # no target
+    assert f(fake, None, fake, 1, 1, 10, 0, 1.0, 0, fake, fake, fake, 1 << 20, None) == ARG       # no draft, T > 0
+    assert f(fake, fake, fake, 0, 1, 10, 0, 1.0, 0, fake, fake, fake, 1 << 20, None) == ARG       # B = 0
+    assert f(fake, fake, fake, 1, 0, 10, 0, 1.0, 0, fake, fake, fake, 1 << 20, None) == ARG       # k = 0
+    assert f(fake, fake, fake, 1, 1, 10, 5, 1.0, 0, fake, fake, fake, 1 << 20, None) == ARG       # dtype
+    assert f(fake, fake, fake, 1, 1, 10, 0, -1.0, 0, fake, fake, fake, 1 << 20, None) == ARG      # T < 0
+    assert f(fake, fake, fake, 1, 1, 10, 0, float("inf"), 0, fake, fake, fake, 1 << 20, None) == ARG
+    assert f(fake, fake, fake, 1, 5000, 10, 0, 1.0, 0, fake, fake, fake, 1 << 20, None) == UNSUP  # k too large
+    assert f(vp(0x10001), fake, fake, 1, 1, 10, 0, 1.0, 0, fake, fake, fake, 1 << 20, None) == ALIGN
+    assert f(fake, fake, fake, 1, 1, 10, 0, 1.0, 0, fake, fake, fake, 16, None) == WS            # too small
+    assert f(fake, fake, fake, 1, 1, 10, 0, 1.0, 0, fake, fake, vp(0x10008), 1 << 20, None) == WS
+    t = lib.spec_verify_tree
+    t.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float,
+                  vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+    assert t(fake, fake, fake, 1, 3, 10, 0, 0.5, fake, fake, None, None, fake, 1 << 20, None) == UNSUP
+    assert t(fake, fake, fake, 1, 5000, 10, 0, 0.0, fake, fake, None, None, fake, 1 << 20, None) == UNSUP
+    assert t(fake, None, fake, 1, 3, 10, 0, 0.0, fake, fake, None, None, fake, 1 << 20, None) == ARG
+
+
+def test_strerror_names_every_code(lib):
+    lib.spec_strerror.restype = ctypes.c_char_p
+    names = {c: lib.spec_strerror(c).decode() for c in range(-8, 1)}
+    assert len(set(names.values())) == 9 and lib.spec_strerror(-99).decode() == "unknown status"

@@ -300,6 +300,25 @@ def test_host_side_argument_errors(sv):
         sv.verify_tree(t, x, x, temperature=0.5)
 
 
+def test_sharded_batch_draws_the_unsharded_randomness(sv):
+    """Shards that pass the index of their first sequence reproduce the whole batch."""
+    from speculative_decoding_draft_online_gb300.sharding import shard_bounds
+    w = wl.c2(seed=55)
+    full = ov.verify_stochastic(w.target, w.draft, w.tokens, w.dtype, w.temperature, 4242)
+    for world in (2, 3):
+        for r in range(world):
+            a, b = shard_bounds(w.B, r, world)
+            t, d = to_device(w.target[a:b], w.dtype), to_device(w.draft[a:b], w.dtype)
+            out, n, aux = sv.verify_ex(t, d, tokens_to_device(w.tokens[a:b]), w.temperature, 4242, aux=True,
+                                       sequence_offset=a)
+            torch.cuda.synchronize()
+            part = ov.verify_stochastic(w.target[a:b], w.draft[a:b], w.tokens[a:b], w.dtype, w.temperature, 4242,
+                                        seq_offset=a)
+            np.testing.assert_array_equal(part.out_tokens, full.out_tokens[a:b])
+            TALLY.add(compare_stochastic(part, out.cpu().numpy(), n.cpu().numpy(), aux["status"].cpu().numpy(),
+                                         w.k))
+
+
 def test_margin_rows_under_one_in_ten_thousand():
     """Positions excused by the margin rule stay under 0.01 % of those compared."""
     if TALLY.rows < 10_000:
