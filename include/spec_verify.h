@@ -170,6 +170,37 @@ int spec_verify_tree(const void* target_logits, const int32_t* node_tokens, cons
 int spec_random(uint64_t seed, int b, int j, int V, float* gumbel_u, float* gumbel_g,
                 float* accept_u, void* cuda_stream);
 
+/*
+ * spec_verify_noalloc -- spec_verify for callers that cannot allocate device
+ * memory.  (The pages describe no such call: this is an interface addition of
+ * this library, not part of the method.)
+ *
+ * Some callers have no device allocator they may use: a plugin inside a host
+ * program that owns all device memory, a runtime whose memory is carved up
+ * before it starts, or a latency-critical path where cudaMalloc's implicit
+ * device synchronisation is not acceptable.  They cannot provide the workspace
+ * spec_verify needs.  This entry point takes no workspace: the kernels use a
+ * fixed array of SPEC_NOALLOC_SCRATCH_BYTES that belongs to the library's
+ * device image, which every GPU that loads the library holds until exit.  It
+ * calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ *   Arguments and results are those of spec_verify (inputs and outputs are
+ *   still the caller's device buffers).
+ *   Sizes whose spec_workspace_size(B, k, V, dtype) exceeds
+ *   SPEC_NOALLOC_SCRATCH_BYTES are rejected with SPEC_ERR_WORKSPACE before any
+ *   launch; use spec_verify with a workspace for those.
+ *   The first call on each device looks up the array's device address (once,
+ *   with that device current); make that first call before any stream capture.
+ *   All calls share the one array per device and it keeps the previous call's
+ *   contents (the library clears what must start at zero), so calls whose work
+ *   may overlap on the GPU -- other streams, other host threads -- race with
+ *   each other: order them on one stream.
+ */
+#define SPEC_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+int spec_verify_noalloc(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
+                        int B, int k, int V, int dtype, float temperature, uint64_t seed,
+                        int32_t* out_tokens, int32_t* out_n_accepted, void* cuda_stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* spec_strerror(int status);
 

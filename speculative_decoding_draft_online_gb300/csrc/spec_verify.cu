@@ -913,3 +913,54 @@ const char* spec_strerror(int status) {
 int spec_abi_version(void) { return (1 << 16) | 0; }
 
 }  // extern "C"
+
+// ------------------------------------------------- allocation-free variant ---
+// spec_verify_noalloc runs the same kernels as spec_verify, with the kernels'
+// scratch (partials, counters, per-row and per-sequence state) in a
+// fixed-size array that is part of this library's device image, so the
+// caller passes no workspace and nothing is allocated at call time.  Every
+// GPU that loads the library holds this array until the process exits.
+namespace sv {
+
+constexpr size_t kNoAllocScratchBytes = SPEC_NOALLOC_SCRATCH_BYTES;
+constexpr int kNoAllocMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of the array on the current device.  The host-side name
+// g_noalloc_scratch is only a stand-in for the symbol, never a device
+// pointer, so the address is looked up once per device, with that device
+// current, and cached.
+static int noalloc_scratch_address(void** out) {
+  static std::mutex mu;
+  static void* addr[kNoAllocMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return SPEC_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return SPEC_ERR_CUDA;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return SPEC_OK;
+}
+
+}  // namespace sv
+
+extern "C" int spec_verify_noalloc(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
+                                   int B, int k, int V, int dtype, float temperature, uint64_t seed,
+                                   int32_t* out_tokens, int32_t* out_n_accepted, void* cuda_stream) {
+  const size_t need = spec_workspace_size(B, k, V, dtype);
+  if (need > sv::kNoAllocScratchBytes) return SPEC_ERR_WORKSPACE;  // sizes beyond the built-in scratch
+  void* scratch = nullptr;
+  const int rc = sv::noalloc_scratch_address(&scratch);
+  if (rc != SPEC_OK) return rc;
+  // The scratch keeps whatever the previous call left in it.  The counters
+  // that must start at zero are returned to zero by every call, and
+  // spec_verify_ex clears the region first whenever the sizes differ from
+  // those of the previous call on this scratch.
+  return spec_verify_ex(target_logits, draft_logits, draft_tokens, B, k, V, dtype, temperature, seed, out_tokens,
+                        out_n_accepted, scratch, sv::kNoAllocScratchBytes, cuda_stream, nullptr);
+}
