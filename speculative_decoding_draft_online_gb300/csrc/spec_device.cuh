@@ -13,9 +13,6 @@ namespace sv {
 
 constexpr int kThreads = 256;          // threads per CTA of every kernel
 constexpr int kWarps = kThreads / 32;
-constexpr int kTile = 2048;            // row pass: partition granularity, elements
-constexpr int kUnroll = 4;             // row pass: 16-byte vectors in flight per thread
-constexpr int kSampleTile = 4096;      // sampling pass: elements per CTA
 
 // ---------------------------------------------------------------- Philox ---
 // Ten rounds of Philox4x32: counter words 0 and 2 are multiplied by two fixed
@@ -95,6 +92,18 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
   return v;
 }
 
+// Order-preserving map from float to unsigned (a < b  <=>  bits(a) < bits(b) for
+// non-NaN floats), so an atomicMax on the bits is a max on the floats; the
+// encoding 0 lies below every float and stands for "none yet".
+__device__ __forceinline__ unsigned ordered_bits(float f) {
+  const unsigned u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float from_ordered(unsigned o) {
+  if (o == 0u) return -CUDART_INF_F;
+  return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
+}
+
 // ---------------------------------------------------- (value, index) order ---
 // a beats b: larger value, then lower index.  Index INT_MAX stands for "none".
 __device__ __forceinline__ bool beats(float va, int ia, float vb, int ib) {
@@ -163,6 +172,101 @@ __device__ __forceinline__ void block_argmax(float& v, int& i, BlockScratch& sh)
   __syncthreads();
   v = bv;
   i = bi;
+}
+
+// (max, sum, bad-flag) over the CTA in one pass: two barriers.
+__device__ __forceinline__ void block_lse_flag(float& m, float& s, int& bad, float c, BlockScratch& sh) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const float M = warp_max(m);
+  s = warp_sum(rescale(s, m, M, c));
+  const int wb = __any_sync(0xffffffffu, bad);
+  if (lane == 0) { sh.f[w] = M; sh.g[w] = s; sh.i[w] = wb; }
+  __syncthreads();
+  const float bm = (lane < kWarps) ? sh.f[lane] : -CUDART_INF_F;
+  float bs = (lane < kWarps) ? sh.g[lane] : 0.f;
+  bad = __any_sync(0xffffffffu, lane < kWarps && sh.i[lane]);
+  const float BM = warp_max(bm);
+  bs = warp_sum(rescale(bs, bm, BM, c));
+  __syncthreads();
+  m = BM;
+  s = bs;
+}
+
+// (value, lowest index, bad-flag) over the CTA in one pass: two barriers.
+__device__ __forceinline__ void block_argmax_flag(float& v, int& i, int& bad, BlockScratch& sh) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  warp_argmax(v, i);
+  const int wb = __any_sync(0xffffffffu, bad);
+  if (lane == 0) { sh.f[w] = v; sh.i[w] = i; sh.g[w] = __int_as_float(wb); }
+  __syncthreads();
+  float bv = (lane < kWarps) ? sh.f[lane] : -CUDART_INF_F;
+  int bi = (lane < kWarps) ? sh.i[lane] : 0x7fffffff;
+  bad = __any_sync(0xffffffffu, lane < kWarps && __float_as_int(sh.g[lane]));
+  warp_argmax(bv, bi);
+  __syncthreads();
+  v = bv;
+  i = bi;
+}
+
+// ------------------------------------------- bulk copies, barriers, flags ---
+__device__ __forceinline__ unsigned smem_addr(const void* p) {
+  return static_cast<unsigned>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+// Make the initialised barriers visible to the bulk-copy engine.
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_addr(bar))
+               : "memory");
+}
+
+// Arrive and announce `bytes` of bulk-copy data that will complete this phase.
+__device__ __forceinline__ void mbar_arrive_tx(uint64_t* bar, unsigned bytes) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
+                   smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
+  unsigned ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// One bulk copy global -> this CTA's shared memory; completion is counted on `bar`.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_addr(dst)),
+               "l"(src), "r"(bytes), "r"(smem_addr(bar))
+               : "memory");
+}
+
+// Order this CTA's earlier shared-memory accesses before later bulk-copy writes.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ int block_or(int x, BlockScratch& sh) {

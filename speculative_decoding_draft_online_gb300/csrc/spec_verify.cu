@@ -11,29 +11,31 @@
 // Speculative Decoding", 3.4.3 "Selecting the accepted tokens"): the longest
 // accepted branch plus the target's next token.
 //
-// The work is a stream over the vocabulary rows, bound by HBM bandwidth:
+// The work is a stream over the vocabulary rows, bound by HBM bandwidth.
 //
-//   row pass     one persistent launch over all rows that need statistics.
-//                Every CTA owns a contiguous range of fixed-size vocabulary
-//                tiles of the (virtual) row list, streams it with 16-byte
-//                no-L1 loads and keeps per-thread running (max, sum of
-//                exp2((x - max) log2e / T)) -- or (max, first index) in greedy
-//                mode -- in registers; a row piece ends in one CTA reduction
-//                and one 8-byte partial.  The CTA that completes a row (atomic
-//                tile count) merges its partials into (max, ln S) or the
-//                argmax; the CTA that completes a sequence runs the per-
-//                sequence step: the accept scan (one warp, one position per
-//                lane, first rejection by ballot), the greedy match, or the
-//                tree walk.  No CTA ever waits for another.
-//   sample pass  stochastic mode only: grid (vocabulary tiles x B).  Each CTA
-//                takes one tile of the row the sequence needs (the rejected
-//                position's target and draft rows, or the bonus row), scores
-//                ln(max(0, p - q)) + Gumbel (or z + Gumbel) with Philox noise
-//                and keeps the best (score, lowest id); the last CTA of a
-//                sequence merges and writes the committed tokens.
+//   row pass    one persistent launch.  Each CTA owns a contiguous range of
+//               4096-element row tiles of the virtual row list (balanced to
+//               one tile) and streams it with 16-byte no-L1 loads, four
+//               vectors per thread in flight at a time.  Threads keep running
+//               (max, sum of exp2((x - max) log2e / T)) -- or (max, first
+//               index) in greedy mode -- across the tiles of a row, one MUFU
+//               ex2 per element;
+//               a row piece ends in one CTA reduction and one 16-byte partial.
+//               The CTA that completes a row (atomic tile count) merges its
+//               partials in one warp; the one that completes a sequence runs
+//               its per-sequence step in that warp: the accept scan (one
+//               position per lane, first rejection by ballot), the greedy
+//               match, or the tree walk.
+//   sampling    stochastic mode, a second launch that starts while the row
+//               pass drains (programmatic dependent launch): one CTA per 8192
+//               ids of the row each sequence needs (the rejected position's
+//               target and draft rows, or the bonus row), scoring
+//               ln max(0, p - q) + Gumbel, or z + Gumbel, with Philox noise,
+//               pruned exactly against the best score reached so far; the
+//               last CTA of a sequence merges and writes the committed tokens.
 //
-// Workspace counters return to zero at the end of every call, so the
-// workspace needs zero-filling only once.
+// No kernel waits on a flag another CTA sets; completion is detected with
+// atomic counters by whichever CTA finishes last.
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -41,6 +43,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 #include <unordered_map>
 
 #include "spec_device.cuh"
@@ -50,16 +53,24 @@ namespace sv {
 
 enum Mode { kStochastic = 0, kGreedy = 1, kTree = 2 };
 
+constexpr int kPartTile = 4096;            // row pass: partition granularity, elements
+constexpr int kUnroll = 4;                 // row pass: 16-byte vectors per thread per batch
+constexpr int kGroups = kPartTile / 4 / kThreads;   // sampling: 4-id groups per thread per tile
+
 struct RowStat {
-  float m;      // max raw logit (stochastic) or the max value (greedy)
-  float lnS;    // ln sum_v exp((x_v - m) / T)
-  int arg;      // argmax, lowest index (greedy / tree)
+  float m;      // max raw logit
+  float lnS;    // ln sum_v exp((x_v - m) / T) (stochastic)
+  int arg;      // index of the max, lowest among equals (greedy and tree)
   int status;   // SPEC_OK or SPEC_ERR_NONFINITE
 };
 
+// One row piece: (max or NaN for bad data, sum relative to the max, index of
+// the max in greedy and tree mode).
 struct Partial {
-  float a;      // piece max (NaN = bad data seen)
-  float b;      // stochastic: sum relative to a; greedy: index bits
+  float m;
+  float s;
+  int idx;
+  int pad;
 };
 
 struct SeqState {
@@ -73,8 +84,9 @@ struct Workspace {
   RowStat* row_stat;       // [R]
   unsigned* seq_cnt;       // [B]
   SeqState* seq;           // [B]
-  Partial* samp_partial;   // [B][nt2]
+  float2* samp_partial;    // [B][ns] (best score or NaN, index bits)
   unsigned* samp_cnt;      // [B]
+  unsigned* samp_floor;    // [B] best score reached so far, order-preserving encoding (0 = none)
 };
 
 struct Params {
@@ -84,10 +96,11 @@ struct Params {
   const int32_t* parents;      // tree only
   int B, k, V;                 // tree: k = N
   int nt;                      // row-pass tiles per row
-  int nt2;                     // sample-pass tiles per row
+  int ns;                      // sampling CTAs per sequence (1 <= ns <= nt)
   int rows_per_seq;            // rows with statistics per sequence
   long long R;                 // rows with statistics
   float invT;                  // 1 / T (stochastic)
+  float T;                     // temperature (stochastic)
   float c;                     // log2(e) / T (stochastic)
   uint2 key;
   uint32_t b0;                 // global index of sequence 0 (Philox counter word 2)
@@ -109,9 +122,9 @@ __device__ __forceinline__ float load_elem<uint16_t>(const uint16_t* p, size_t i
 template <>
 __device__ __forceinline__ float load_elem<float>(const float* p, size_t i) { return __ldg(p + i); }
 
-// Virtual row r of the row pass -> its address and its sequence.
-// Stochastic: per sequence, target rows 0..k-1 then draft rows 0..k-1 (the
-// bonus row k needs no normaliser).  Greedy / tree: the sequence's target rows.
+// Virtual row r -> its address and its sequence.  Stochastic: per sequence,
+// target rows 0..k-1 then draft rows 0..k-1 (the bonus row k needs no
+// normaliser).  Greedy / tree: the sequence's target rows.
 template <typename T, int kMode>
 __device__ __forceinline__ const T* row_ptr(const Params& P, long long r, int& b) {
   if constexpr (kMode == kStochastic) {
@@ -166,10 +179,23 @@ struct Vec<float> {
   }
 };
 
-// Running max m of the raw logits and sums s_j = sum exp2((x - m) c), c = log2(e)/T.
-// The max of each chunk is found first (packed max on the raw data), so each
-// element costs one FFMA, one MUFU ex2 and one add; the sums are rescaled only
-// when the running max rises.
+// First index of value cm among the vectors' elements (it is there).
+template <typename T, int U>
+__device__ __forceinline__ int first_index_of(const uint4 (&v)[U], const int (&idx)[U], float cm) {
+#pragma unroll
+  for (int u = 0; u < U; ++u)
+#pragma unroll
+    for (int e = 0; e < Vec<T>::n; ++e)
+      if (Vec<T>::at(v[u], e) == cm) return idx[u] + e;
+  return INT_MAX;
+}
+
+// Running max m of the raw logits and sums s_j = sum exp2((x - m) c),
+// c = log2(e)/T.  The max of each chunk is found first (packed max on the raw
+// data), so each element costs one FFMA, one MUFU ex2 and one add; the sums
+// are rescaled only when the running max rises.  (The index of the max is not
+// tracked: searching for it whenever some lane's max rises costs more than
+// the rest of the fold.)
 struct LseAcc {
   float c, m, mc;
   float s[8];
@@ -182,27 +208,28 @@ struct LseAcc {
     for (int j = 0; j < 8; ++j) s[j] = 0.f;
     bad = 0;
   }
-  __device__ __forceinline__ bool raise(float cm) {
-    if (cm != cm) { bad = 1; return false; }
-    if (cm > m) {
-      const float f = ex2_approx((m - cm) * c);
+  __device__ __forceinline__ void rise(float cm) {
+    const float f = ex2_approx((m - cm) * c);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) s[j] *= f;
-      m = cm;
-      mc = m * c;
-    }
-    return m != -CUDART_INF_F;
+    for (int j = 0; j < 8; ++j) s[j] *= f;
+    m = cm;
+    mc = m * c;
   }
   template <typename T, int U>
   __device__ __forceinline__ void vec(const uint4 (&v)[U], const int (&)[U]) {
-    if (!raise(Vec<T>::template nanmax_all<U>(v))) return;
+    const float cm = Vec<T>::template nanmax_all<U>(v);
+    if (cm != cm) { bad = 1; return; }
+    if (cm > m) rise(cm);
+    if (m == -CUDART_INF_F) return;
 #pragma unroll
     for (int u = 0; u < U; ++u)
 #pragma unroll
       for (int e = 0; e < Vec<T>::n; ++e) s[e] += ex2_approx(fmaf(Vec<T>::at(v[u], e), c, -mc));
   }
   __device__ __forceinline__ void scalar(float x, int) {
-    if (raise(x)) s[0] += ex2_approx(fmaf(x, c, -mc));
+    if (x != x) { bad = 1; return; }
+    if (x > m) rise(x);
+    if (m != -CUDART_INF_F) s[0] += ex2_approx(fmaf(x, c, -mc));
   }
   __device__ float sum() const {
     return ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
@@ -226,15 +253,8 @@ struct ArgmaxAcc {
     const float cm = Vec<T>::template nanmax_all<U>(v);
     if (cm != cm) { bad = 1; return; }
     if (cm > bv || bi == INT_MAX) {
-#pragma unroll
-      for (int u = 0; u < U; ++u)
-#pragma unroll
-        for (int e = 0; e < Vec<T>::n; ++e)
-          if (Vec<T>::at(v[u], e) == cm) {
-            bv = cm;
-            bi = idx[u] + e;
-            return;
-          }
+      bv = cm;
+      bi = first_index_of<T, U>(v, idx, cm);
     }
   }
   __device__ __forceinline__ void scalar(float x, int i) {
@@ -243,31 +263,37 @@ struct ArgmaxAcc {
   }
 };
 
-// Stream elements [e0, e1) of one row through `acc`: scalar head up to the
-// first 16-byte boundary, 16-byte vectors kUnroll at a time (each load
-// coalesced across the warp), then the vector remainder and a scalar tail.
+// Stream elements [e0, e1) of one row through `acc`: a scalar head up to the
+// first 16-byte boundary, then 16-byte vectors kUnroll per thread per batch
+// (each load coalesced across the warp; all of a batch's loads are issued
+// before it is folded), then the vector remainder and a scalar tail.  Four
+// CTAs of 64 registers per SM keep enough loads in flight; a software
+// pipeline that requests the next batch early needs more registers, and the
+// occupancy it costs loses more than it gains.
+// Each thread sees its elements in increasing index order.
 template <typename T, class Acc>
 __device__ __forceinline__ void scan_segment(const T* row, int e0, int e1, Acc& acc) {
   constexpr int kVec = Vec<T>::n;
+  constexpr int kBatch = kUnroll * kThreads;   // vectors per CTA per batch
   const int tid = threadIdx.x;
   const uintptr_t addr = reinterpret_cast<uintptr_t>(row + e0);
-  int head = (int)(((16u - (unsigned)(addr & 15u)) & 15u) / sizeof(T));
-  head = min(head, e1 - e0);
+  const int head = min((int)(((16u - (unsigned)(addr & 15u)) & 15u) / sizeof(T)), e1 - e0);
   if (tid < head) acc.scalar(load_elem<T>(row, e0 + tid), e0 + tid);
   const int vb = e0 + head;
   const int nvec = (e1 - vb) / kVec;
   const uint4* vp = reinterpret_cast<const uint4*>(row + vb);
-  int j = tid;
-  for (; j + (kUnroll - 1) * kThreads < nvec; j += kUnroll * kThreads) {
+  const int nfull = nvec / kBatch;
+  for (int bt = 0; bt < nfull; ++bt) {
+    const int base = bt * kBatch + tid;
     uint4 v[kUnroll];
     int idx[kUnroll];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) v[u] = ld_stream16(vp + j + u * kThreads);
+    for (int u = 0; u < kUnroll; ++u) v[u] = ld_stream16(vp + base + u * kThreads);
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) idx[u] = vb + (j + u * kThreads) * kVec;
+    for (int u = 0; u < kUnroll; ++u) idx[u] = vb + (base + u * kThreads) * kVec;
     acc.template vec<T, kUnroll>(v, idx);
   }
-  for (; j < nvec; j += kThreads) {
+  for (int j = nfull * kBatch + tid; j < nvec; j += kThreads) {
     uint4 v[1] = {ld_stream16(vp + j)};
     int idx[1] = {vb + j * kVec};
     acc.template vec<T, 1>(v, idx);
@@ -286,9 +312,10 @@ __device__ __forceinline__ void stcg_stat(RowStat* p, const RowStat& s) {
 }
 
 // --------------------------------------------------- per-sequence steps ---
+// All of these run in warp 0 of the CTA that completed the sequence.
 
-// Accept scan of one sequence (warp 0): lane i evaluates position i of each
-// 32-position chunk; the first rejection is the lowest set bit of the ballot.
+// Accept scan: lane i evaluates position i of each 32-position chunk; the
+// first rejection is the lowest set bit of the ballot.
 template <typename T>
 __device__ void accept_scan(const Params& P, int b) {
   const int lane = threadIdx.x & 31;
@@ -329,11 +356,11 @@ __device__ void accept_scan(const Params& P, int b) {
   }
   if (lane == 0) {
     const int st = tok_bad ? SPEC_ERR_TOKEN : nf_bad ? SPEC_ERR_NONFINITE : SPEC_OK;
-    P.ws.seq[b] = SeqState{n, st};
+    __stcg(reinterpret_cast<int2*>(P.ws.seq) + b, make_int2(n, st));
   }
 }
 
-// Greedy match of one sequence (warp 0): n = first i with x_i != argmax_i.
+// Greedy match: n = first i with x_i != argmax_i.
 __device__ void greedy_match(const Params& P, int b) {
   const int lane = threadIdx.x & 31;
   const int k = P.k;
@@ -370,19 +397,17 @@ __device__ void greedy_match(const Params& P, int b) {
   }
 }
 
-// Greedy tree verification of one sequence (whole CTA).  Node m is accepted iff
-// its parent is (the context is) and its token is the argmax of the parent's
-// row; the deepest accepted node wins, the lowest index among equals.
+// Greedy tree verification.  Node m is accepted iff its parent is (the context
+// is) and its token is the argmax of the parent's row; the deepest accepted
+// node wins, the lowest index among equals.
 __device__ void tree_walk(const Params& P, int b) {
   __shared__ short s_par[SPEC_MAX_TREE_N];
-  __shared__ short s_dep[SPEC_MAX_TREE_N];  // depth if accepted, 0 if not; ok flag before the walk
-  __shared__ int s_best, s_bad;
+  __shared__ short s_dep[SPEC_MAX_TREE_N];  // ok flag, then depth if accepted (0 if not)
+  const int lane = threadIdx.x & 31;
   const int N = P.k;
   const long long rbase = (long long)b * (N + 1);
-  if (threadIdx.x == 0) s_bad = 0;
-  __syncthreads();
   int tbad = 0, fbad = 0;
-  for (int m = threadIdx.x; m < N; m += kThreads) {
+  for (int m = lane; m < N; m += 32) {
     const int par = P.parents[(size_t)b * N + m];
     const int tok = P.tokens[(size_t)b * N + m];
     const bool ok_shape = par >= -1 && par < m && tok >= 0 && tok < P.V;
@@ -392,12 +417,12 @@ __device__ void tree_walk(const Params& P, int b) {
     s_par[m] = (short)(ok_shape ? par : -1);
     s_dep[m] = (short)ok;
   }
-  for (int r = threadIdx.x; r <= N; r += kThreads) fbad |= ldcg_stat(P.ws.row_stat + rbase + r).status != SPEC_OK;
-  if (tbad) atomicOr(&s_bad, 2);
-  if (fbad) atomicOr(&s_bad, 1);
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int best = -1, best_d = 0;
+  for (int r = lane; r <= N; r += 32) fbad |= ldcg_stat(P.ws.row_stat + rbase + r).status != SPEC_OK;
+  tbad = __any_sync(0xffffffffu, tbad);
+  fbad = __any_sync(0xffffffffu, fbad);
+  __syncwarp();
+  int best = -1, best_d = 0;
+  if (lane == 0) {
     for (int m = 0; m < N; ++m) {
       const int par = s_par[m];
       int d = 0;
@@ -405,84 +430,85 @@ __device__ void tree_walk(const Params& P, int b) {
       s_dep[m] = (short)d;
       if (d > best_d) { best_d = d; best = m; }
     }
-    s_best = best;
   }
-  __syncthreads();
-  const int st = (s_bad & 2) ? SPEC_ERR_TOKEN : (s_bad & 1) ? SPEC_ERR_NONFINITE : SPEC_OK;
-  const int best = s_best;
-  const int depth = best < 0 ? 0 : s_dep[best];
+  best = __shfl_sync(0xffffffffu, best, 0);
+  best_d = __shfl_sync(0xffffffffu, best_d, 0);
+  __syncwarp();
+  const int st = tbad ? SPEC_ERR_TOKEN : fbad ? SPEC_ERR_NONFINITE : SPEC_OK;
   int32_t* out = P.out_tokens + (size_t)b * (N + 1);
-  for (int i = threadIdx.x; i <= N; i += kThreads)
-    if (st != SPEC_OK || i > depth) out[i] = -1;
-  if (threadIdx.x == 0 && st == SPEC_OK) {
-    out[depth] = ldcg_stat(P.ws.row_stat + rbase + (best < 0 ? 0 : best + 1)).arg;
-    for (int m = best, d = depth - 1; m >= 0; m = s_par[m], --d) out[d] = P.tokens[(size_t)b * N + m];
-  }
-  if (threadIdx.x == 0) {
-    P.out_n[b] = st == SPEC_OK ? depth : -1;
+  for (int i = lane; i <= N; i += 32)
+    if (st != SPEC_OK || i > best_d) out[i] = -1;
+  if (lane == 0) {
+    if (st == SPEC_OK) {
+      out[best_d] = ldcg_stat(P.ws.row_stat + rbase + (best < 0 ? 0 : best + 1)).arg;
+      for (int m = best, d = best_d - 1; m >= 0; m = s_par[m], --d) out[d] = P.tokens[(size_t)b * N + m];
+    }
+    P.out_n[b] = st == SPEC_OK ? best_d : -1;
     if (P.out_leaf) P.out_leaf[b] = st == SPEC_OK ? best : -1;
     if (P.status) P.status[b] = st;
   }
 }
 
-// --------------------------------------------------------------- row pass ---
-
+// A row's last piece has landed: merge its partials into the row statistics
+// (warp 0); if that completes the sequence, run its per-sequence step.
 template <typename T, int kMode>
-__device__ void finish_row(const Params& P, long long r, int b, BlockScratch& sh, int& s_last) {
+__device__ void finish_row(const Params& P, long long r, int b) {
+  const int lane = threadIdx.x & 31;
   __threadfence();
-  const Partial* src = P.ws.row_partial + r * P.nt;
-  RowStat st;
-  if constexpr (kMode == kStochastic) {
-    float m = -CUDART_INF_F, s = 0.f;
-    int bad = 0;
-    for (int t = threadIdx.x; t < P.nt; t += kThreads) {
-      const float2 p = __ldcg(reinterpret_cast<const float2*>(src + t));
-      if (p.x != p.x) { bad = 1; continue; }
+  const float4* src = reinterpret_cast<const float4*>(P.ws.row_partial + r * P.nt);
+  float m = -CUDART_INF_F, s = 0.f;
+  int ix = INT_MAX, bad = 0;
+  for (int t = lane; t < P.nt; t += 32) {
+    const float4 p = __ldcg(src + t);
+    if (p.x != p.x) { bad = 1; continue; }
+    if constexpr (kMode == kStochastic) {
       const float M = fmaxf(m, p.x);
       s = rescale(s, m, M, P.c) + rescale(p.y, p.x, M, P.c);
-      m = M;
+    } else {
+      const int pi = __float_as_int(p.z);
+      if (beats(p.x, pi, m, ix)) ix = pi;
     }
-    bad = block_or(bad, sh);
-    block_lse(m, s, P.c, sh);
-    const bool finite = m > -CUDART_INF_F && m < CUDART_INF_F && s > 0.f && s < CUDART_INF_F;
-    st = RowStat{m, logf(s), 0, (bad || !finite) ? SPEC_ERR_NONFINITE : SPEC_OK};
-  } else {
-    float v = -CUDART_INF_F;
-    int ix = INT_MAX, bad = 0;
-    for (int t = threadIdx.x; t < P.nt; t += kThreads) {
-      const float2 p = __ldcg(reinterpret_cast<const float2*>(src + t));
-      if (p.x != p.x) { bad = 1; continue; }
-      const int pi = __float_as_int(p.y);
-      if (beats(p.x, pi, v, ix)) { v = p.x; ix = pi; }
-    }
-    bad = block_or(bad, sh);
-    block_argmax(v, ix, sh);
-    st = RowStat{v, 0.f, ix, bad ? SPEC_ERR_NONFINITE : SPEC_OK};
+    m = fmaxf(m, p.x);
   }
-  if (threadIdx.x == 0) {
+  RowStat st;
+  if constexpr (kMode == kStochastic) {
+    const float M = warp_max(m);
+    s = warp_sum(rescale(s, m, M, P.c));
+    bad = __any_sync(0xffffffffu, bad);
+    const bool finite = M > -CUDART_INF_F && M < CUDART_INF_F && s > 0.f && s < CUDART_INF_F;
+    st = RowStat{M, logf(s), INT_MAX, (bad || !finite) ? SPEC_ERR_NONFINITE : SPEC_OK};
+  } else {
+    warp_argmax(m, ix);
+    bad = __any_sync(0xffffffffu, bad);
+    st = RowStat{m, 0.f, ix, bad ? SPEC_ERR_NONFINITE : SPEC_OK};
+  }
+  int last = 0;
+  if (lane == 0) {
     stcg_stat(P.ws.row_stat + r, st);
     P.ws.row_cnt[r] = 0;  // ready for the next call
     __threadfence();
     const unsigned old = atomicAdd(P.ws.seq_cnt + b, 1u);
-    s_last = old + 1 == (unsigned)P.rows_per_seq;
-    if (s_last) P.ws.seq_cnt[b] = 0;
+    last = old + 1 == (unsigned)P.rows_per_seq;
+    if (last) P.ws.seq_cnt[b] = 0;
   }
-  __syncthreads();
-  if (s_last) {
-    __threadfence();
-    if constexpr (kMode == kTree) {
-      tree_walk(P, b);
-    } else if (threadIdx.x < 32) {
-      if constexpr (kMode == kStochastic) accept_scan<T>(P, b);
-      else greedy_match(P, b);
-    }
-  }
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (!last) return;
+  __threadfence();
+  if constexpr (kMode == kTree) tree_walk(P, b);
+  else if constexpr (kMode == kStochastic) accept_scan<T>(P, b);
+  else greedy_match(P, b);
 }
+
+// --------------------------------------------------------------- row pass ---
 
 template <typename T, int kMode>
 __global__ void __launch_bounds__(kThreads) row_pass_kernel(const Params P) {
   __shared__ BlockScratch sh;
-  __shared__ int s_last;
+  // the sampling launch may be scheduled as this grid's CTAs retire; it waits
+  // for this grid's results before reading them
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (threadIdx.x == 0) sh.flag = 0;
+  __syncthreads();
   const long long I = P.R * P.nt;
   const long long i0 = I * blockIdx.x / gridDim.x;
   const long long i1 = I * (blockIdx.x + 1) / gridDim.x;
@@ -492,133 +518,467 @@ __global__ void __launch_bounds__(kThreads) row_pass_kernel(const Params P) {
     const int t1 = (int)min((long long)P.nt, (long long)t0 + (i1 - i));
     int b;
     const T* row = row_ptr<T, kMode>(P, r, b);
-    const int e0 = t0 * kTile, e1 = min(P.V, t1 * kTile);
-    float2 part;
+    const int e0 = t0 * kPartTile, e1 = min(P.V, t1 * kPartTile);
+    float4 part;
     if constexpr (kMode == kStochastic) {
       LseAcc acc;
       acc.init(P.c);
       scan_segment<T>(row, e0, e1, acc);
       float m = acc.m, s = acc.sum();
-      const int bad = block_or(acc.bad, sh);
-      block_lse(m, s, P.c, sh);
-      part = make_float2(bad ? CUDART_NAN_F : m, s);
+      int bad = acc.bad;
+      block_lse_flag(m, s, bad, P.c, sh);
+      part = make_float4(bad ? CUDART_NAN_F : m, s, __int_as_float(INT_MAX), 0.f);
     } else {
       ArgmaxAcc acc;
       acc.init();
       scan_segment<T>(row, e0, e1, acc);
       float v = acc.bv;
-      int ix = acc.bi;
-      const int bad = block_or(acc.bad, sh);
-      block_argmax(v, ix, sh);
-      part = make_float2(bad ? CUDART_NAN_F : v, __int_as_float(ix));
+      int ix = acc.bi, bad = acc.bad;
+      block_argmax_flag(v, ix, bad, sh);
+      part = make_float4(bad ? CUDART_NAN_F : v, 0.f, __int_as_float(ix), 0.f);
     }
-    if (threadIdx.x == 0) {
-      float2* dst = reinterpret_cast<float2*>(P.ws.row_partial + r * P.nt);
-      __stcg(dst + t0, part);
-      const float2 neutral = make_float2(-CUDART_INF_F, kMode == kStochastic ? 0.f : __int_as_float(INT_MAX));
-      for (int t = t0 + 1; t < t1; ++t) __stcg(dst + t, neutral);
-      __threadfence();
-      const unsigned add = (unsigned)(t1 - t0);
-      const unsigned old = atomicAdd(P.ws.row_cnt + r, add);
-      s_last = old + add == (unsigned)P.nt;
+    if (threadIdx.x < 32) {
+      int last = 0;
+      if (threadIdx.x == 0) {
+        float4* dst = reinterpret_cast<float4*>(P.ws.row_partial + r * P.nt);
+        __stcg(dst + t0, part);
+        // the piece's other tiles: nothing to add to the sums or the argmax
+        const float4 neutral = make_float4(-CUDART_INF_F, 0.f, __int_as_float(INT_MAX), 0.f);
+        for (int u = t0 + 1; u < t1; ++u) __stcg(dst + u, neutral);
+        __threadfence();
+        const unsigned add = (unsigned)(t1 - t0);
+        last = atomicAdd(P.ws.row_cnt + r, add) + add == (unsigned)P.nt;
+      }
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (last) finish_row<T, kMode>(P, r, b);
     }
-    __syncthreads();
-    if (s_last) finish_row<T, kMode>(P, r, b, sh, s_last);
     __syncthreads();
     i += t1 - t0;
   }
 }
 
-// ------------------------------------------------------------ sample pass ---
+// ------------------------------------------------------------ sampling ---
+//
+// Gumbel noise is bounded above: U <= 1 - 2^-24 gives G < 16.64.  An id whose
+// score bound -- ln p_v for the residual (ln(p - q) <= ln p), z_v = x_v / T for
+// the bonus -- plus that bound stays below a score some id reaches cannot win,
+// so its noise is never drawn.  Each thread scores the candidate with its own
+// best bound; the CTA's floor is the best of those scores and of what the
+// sequence's other tiles had published when this one started (atomic max,
+// nothing waits for it).  An id that passes the bound meets a cheap
+// conservative test on its uniform before the accurate logarithms.  The result
+// is the unpruned argmax, ties included.
+//
+// For the residual the kernel works with delta_v = ln q_v - ln p_v =
+// ((x_d - x_t) - (m_d - m_t)) / T - (lnS_d - lnS_t): an id is a candidate iff
+// delta_v < 0, and ln(p - q) = ln p + ln(-expm1(delta)).
+constexpr float kGumbelMax = 16.7f;      // > -ln(-ln(1 - 2^-24)) = 16.6355
+constexpr float kPruneSlack = 1e-3f;     // covers the fp32 error of the fast test
+
+// May a draw from uniform u lift a score bound h to `floor`?  G(u) >= need holds
+// iff u >= exp(-exp(-need)); the fast exponentials are off by far less than the
+// slack and the 3e-5 relative allowance, so every id that can reach is kept.
+__device__ __forceinline__ bool may_reach(float u, float h, float floor) {
+  const float need = floor - h - kPruneSlack;
+  return u >= __expf(-__expf(-need)) * (1.0f - 3e-5f);
+}
+
+// Four consecutive logits: 8 bytes of bf16 or 16 bytes of fp32.
+template <typename T>
+struct Raw4 {
+  uint32_t w[sizeof(T)];
+};
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads) sample_pass_kernel(const Params P) {
-  __shared__ BlockScratch sh;
-  __shared__ int s_last;
-  const int b = blockIdx.x / P.nt2;
-  const int t = blockIdx.x % P.nt2;
-  const int k = P.k;
-  const SeqState ss = P.ws.seq[b];
-  const int n = ss.n;
-  float best = -CUDART_INF_F;
-  int bidx = INT_MAX, bad = 0;
-  const int v0 = t * kSampleTile, v1 = min(P.V, v0 + kSampleTile);
-  if (ss.status == SPEC_OK) {
-    if (n < k) {
-      // residual: ln(p - q) = ln p + ln(1 - exp(ln q - ln p)) where p > q
-      const RowStat rt = ldcg_stat(P.ws.row_stat + (long long)b * 2 * k + n);
-      const RowStat rd = ldcg_stat(P.ws.row_stat + (long long)b * 2 * k + k + n);
-      const T* trow = (const T*)P.target + ((size_t)b * (k + 1) + n) * P.V;
-      const T* drow = (const T*)P.draft + ((size_t)b * k + n) * P.V;
-      for (int g = (v0 >> 2) + threadIdx.x; 4 * g < v1; g += kThreads) {
-        const uint4 w = gumbel_words(P.key, P.b0 + (uint32_t)b, n, (uint32_t)g);
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int v = 4 * g + e;
-          if (v >= v1) break;
-          const float lp = (load_elem<T>(trow, v) - rt.m) * P.invT - rt.lnS;
-          const float lq = (load_elem<T>(drow, v) - rd.m) * P.invT - rd.lnS;
-          if (lp > lq) {
-            const float sc = lp + logf(-expm1f(lq - lp)) + gumbel_of(uniform_of(ws[e]));
-            if (beats(sc, v, best, bidx)) { best = sc; bidx = v; }
-          }
-        }
-      }
+__device__ __forceinline__ Raw4<T> lds_raw4(const T* p) {
+  Raw4<T> r;
+  if constexpr (sizeof(T) == 2) {
+    const uint2 w = *reinterpret_cast<const uint2*>(p);
+    r.w[0] = w.x;
+    r.w[1] = w.y;
+  } else {
+    const uint4 w = *reinterpret_cast<const uint4*>(p);
+    r.w[0] = w.x; r.w[1] = w.y; r.w[2] = w.z; r.w[3] = w.w;
+  }
+  return r;
+}
+
+template <typename T>
+__device__ __forceinline__ float raw_at(const Raw4<T>& r, int e) {
+  if constexpr (sizeof(T) == 2) return (e & 1) ? bf16_hi(r.w[e >> 1]) : bf16_lo(r.w[e >> 1]);
+  else return __uint_as_float(r.w[e]);
+}
+
+// NaN-propagating max of the first `cnt` (1..4) logits of a group (bf16, all
+// four: one packed max).
+template <typename T>
+__device__ __forceinline__ float group_max(const Raw4<T>& r, int cnt) {
+  if (cnt >= 4) {
+    if constexpr (sizeof(T) == 2) {
+      const uint32_t m = bf16x2_nanmax(r.w[0], r.w[1]);
+      return nanmax(bf16_lo(m), bf16_hi(m));
     } else {
-      // bonus: argmax of x/T + Gumbel over target row k
-      const T* trow = (const T*)P.target + ((size_t)b * (k + 1) + k) * P.V;
-      for (int g = (v0 >> 2) + threadIdx.x; 4 * g < v1; g += kThreads) {
-        const uint4 w = gumbel_words(P.key, P.b0 + (uint32_t)b, k, (uint32_t)g);
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+      return nanmax(nanmax(__uint_as_float(r.w[0]), __uint_as_float(r.w[1])),
+                    nanmax(__uint_as_float(r.w[2]), __uint_as_float(r.w[3])));
+    }
+  }
+  float m = raw_at<T>(r, 0);
+  for (int e = 1; e < cnt; ++e) m = nanmax(m, raw_at<T>(r, e));
+  return m;
+}
+
+// What a sampling CTA knows about its sequence's row.
+struct SampleRow {
+  bool resid;
+  float mt, lnSt;       // target row statistics (residual)
+  float cdelta;         // delta_v = fma(x_d - x_t, 1/T, cdelta)
+};
+
+// Exact score of id v (or -inf if it is no candidate) from its logits and noise uniform.
+__device__ __forceinline__ float exact_score(float invT, const SampleRow& R, float xt, float xd, float u) {
+  if (R.resid) {
+    const float delta = fmaf(xd - xt, invT, R.cdelta);
+    if (!(delta < 0.f)) return -CUDART_INF_F;
+    const float lp = (xt - R.mt) * invT - R.lnSt;
+    return lp + logf(-expm1f(delta)) + gumbel_of(u);
+  }
+  if (!(xt > -CUDART_INF_F)) return -CUDART_INF_F;
+  return xt * invT + gumbel_of(u);
+}
+
+__device__ __forceinline__ float uniform_at(uint2 key, uint32_t b, int j, int v) {
+  const uint4 w = gumbel_words(key, b, j, (uint32_t)(v >> 2));
+  const int e = v & 3;
+  return uniform_of(e == 0 ? w.x : e == 1 ? w.y : e == 2 ? w.z : w.w);
+}
+
+// What a sampling thread knows about its sequence's draw.
+struct Draw {
+  float invT, T;
+  SampleRow R;
+  uint2 key;
+  uint32_t gb;            // Philox counter word 2: the sequence's global index
+  int j;                  // Philox counter word 1: the row whose noise is drawn
+};
+
+// Candidate test and score bound of one id: ln p for the residual, z for the bonus.
+__device__ __forceinline__ bool bound_of(const Draw& D, float x, float xdv, float& h) {
+  if (D.R.resid) {
+    h = (x - D.R.mt) * D.invT - D.R.lnSt;
+    return fmaf(xdv - x, D.invT, D.R.cdelta) < 0.f;
+  }
+  h = x * D.invT;
+  return x > -CUDART_INF_F;
+}
+
+// The lowest target logit that can still reach score fl: bound + G_max >= fl.
+__device__ __forceinline__ float threshold_of(const Draw& D, float fl) {
+  if (!(fl > -CUDART_INF_F)) return -CUDART_INF_F;
+  return D.R.resid ? D.R.mt + (fl - kGumbelMax + D.R.lnSt) * D.T : (fl - kGumbelMax) * D.T;
+}
+
+// Shared memory of a sampling CTA: a ring of tiles (target and draft logits
+// of 4096 ids each), filled by bulk copies, and each warp's queue of groups
+// whose noise is to be drawn.
+template <typename T>
+struct SampleSmem {
+  static constexpr int kStages = sizeof(T) == 2 ? 3 : 2;
+  T tile[kStages][2][kPartTile];
+  uint64_t bar[kStages];
+  uint32_t queue[kWarps][kGroups * 32];
+};
+
+// Score the ids of tile [v0, v1) (staged at st / sd) that can reach the
+// floor.  Thread g owns groups g, g + kThreads, ...; a group whose largest
+// target logit reaches the threshold goes into the warp's queue, and the
+// warp's lanes share the queued groups out: the id-by-id bound and candidate
+// tests, and the noise draw of a group with an id that passes them, run only
+// there, one group per lane, so no lane waits on another's groups.
+template <typename T>
+__device__ __forceinline__ void score_tile(const Draw& D, int v0, int v1, const T* st, const T* sd,
+                                           uint32_t* queue, float& floor, float& best, int& bidx, int& bad) {
+  const int lane = threadIdx.x & 31;
+  const float xthr = threshold_of(D, floor);
+  const int nv = v1 - v0;
+  int cnt = 0;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int v = 4 * g + e;
-          if (v >= v1) break;
-          const float x = load_elem<T>(trow, v);
-          if (x != x || x == CUDART_INF_F) bad = 1;
-          const float sc = x * P.invT + gumbel_of(uniform_of(ws[e]));
-          if (beats(sc, v, best, bidx)) { best = sc; bidx = v; }
-        }
+  for (int q = 0; q < kGroups; ++q) {
+    const int o = 4 * (q * kThreads + threadIdx.x);
+    bool hit = false;
+    if (o < nv) {
+      const float gm = group_max<T>(lds_raw4<T>(st + o), min(4, nv - o));
+      if (!D.R.resid && !(gm < CUDART_INF_F)) bad = 1;     // NaN or +inf in the bonus row
+      hit = gm >= xthr;
+    }
+    const unsigned need = __ballot_sync(0xffffffffu, hit);
+    if (hit) queue[cnt + __popc(need & ((1u << lane) - 1u))] = (uint32_t)o;
+    cnt += __popc(need);
+  }
+  __syncwarp();
+  for (int it = lane; it < cnt; it += 32) {
+    const int o = (int)queue[it];
+    const int v = v0 + o;
+    const int ne = min(4, nv - o);
+    const Raw4<T> gt = lds_raw4<T>(st + o);
+    Raw4<T> gd;
+    if (D.R.resid) gd = lds_raw4<T>(sd + o);
+    unsigned pass = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float x = raw_at<T>(gt, e);
+      float h;
+      if (e < ne && x >= xthr && bound_of(D, x, D.R.resid ? raw_at<T>(gd, e) : 0.f, h)) pass |= 1u << e;
+    }
+    if (!pass) continue;
+    const uint4 w = gumbel_words(D.key, D.gb, D.j, (uint32_t)(v >> 2));
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (!((pass >> e) & 1u)) continue;
+      const float x = raw_at<T>(gt, e);
+      const float xdv = D.R.resid ? raw_at<T>(gd, e) : 0.f;
+      float h;
+      bound_of(D, x, xdv, h);
+      const float u = uniform_of(ws[e]);
+      if (!may_reach(u, h, floor)) continue;
+      const float sc = exact_score(D.invT, D.R, x, xdv, u);
+      if (beats(sc, v + e, best, bidx)) {
+        best = sc;
+        bidx = v + e;
+        floor = fmaxf(floor, sc);
       }
     }
   }
-  bad = block_or(bad, sh);
-  block_argmax(best, bidx, sh);
+  __syncwarp();   // the queue is refilled by the next tile
+}
+
+constexpr long long kWaitLimitNs = 1000000000LL;   // 1 s: a bulk copy that has not landed by then never will
+
+__device__ __forceinline__ long long global_ns() {
+  long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for phase `parity` of `bar`; false if it did not complete within the limit.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = global_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  return true;
+}
+
+// One sequence's draw runs on ns CTAs over the row pass's 4096-id tiles.
+//
+//   1. floor: the first tile a CTA scores is the one whose row piece holds
+//      the target row's max (the bonus row has no statistics: the CTA's own
+//      first tile).  Each thread scores the candidate with its best bound
+//      there, and the CTA takes the best of those scores and of what the
+//      sequence's other CTAs have published.  Every CTA starts near the top
+//      of the distribution for one extra tile read (mostly from L2), and none
+//      waits for another.
+//   2. CTA c scores tiles c, c + ns, ...  Tiles reach shared memory through
+//      bulk copies kStages ahead of use, so the loads of a CTA's tiles are in
+//      flight together (rows whose tiles do not meet the bulk copy's 16-byte
+//      rules are loaded by the threads, one tile at a time).
+//   3. per-CTA (best, index) partials; the sequence's last CTA merges them and
+//      writes the committed tokens.
+template <typename T>
+__global__ void __launch_bounds__(kThreads) sample_kernel(const Params P) {
+  using Smem = SampleSmem<T>;
+  constexpr int kStages = Smem::kStages;
+  extern __shared__ __align__(128) unsigned char dyn_smem[];
+  Smem& S = *reinterpret_cast<Smem*>(dyn_smem);
+  __shared__ BlockScratch sh;
+  __shared__ float s_floor[kWarps];
+  __shared__ int s_last, s_timeout;
   if (threadIdx.x == 0) {
-    __stcg(reinterpret_cast<float2*>(P.ws.samp_partial) + (size_t)b * P.nt2 + t,
-           make_float2(bad ? CUDART_NAN_F : best, __int_as_float(bidx)));
+    for (int i = 0; i < kStages; ++i) mbar_init(&S.bar[i], 1);
+    fence_mbar_init();
+    s_timeout = 0;
+  }
+  // the row pass's statistics and sequence states must be visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int b = blockIdx.x / P.ns;
+  const int c = blockIdx.x % P.ns;
+  const int k = P.k;
+  const int2 sv2 = __ldcg(reinterpret_cast<const int2*>(P.ws.seq) + b);
+  const int n = sv2.x, status = sv2.y;
+  const bool active = status == SPEC_OK;            // uniform over the CTA
+  Draw D;
+  D.invT = P.invT;
+  D.T = P.T;
+  D.key = P.key;
+  D.gb = P.b0 + (uint32_t)b;
+  D.j = n < k ? n : k;
+  D.R.resid = n < k;
+  D.R.mt = D.R.lnSt = D.R.cdelta = 0.f;
+  const T* trow = (const T*)P.target + ((size_t)b * (k + 1) + (active ? D.j : 0)) * P.V;
+  const T* drow = D.R.resid ? (const T*)P.draft + ((size_t)b * k + (active ? n : 0)) * P.V : nullptr;
+  // bulk copies need 16-byte aligned rows and tiles of whole 16-byte units
+  const bool bulk = (reinterpret_cast<uintptr_t>(trow) % 16 == 0) &&
+                    (!drow || reinterpret_cast<uintptr_t>(drow) % 16 == 0) &&
+                    ((size_t)P.V * sizeof(T)) % 16 == 0;
+  // tiles in the order they are scored: residual [floor tile, c, c + ns, ...],
+  // bonus [c, c + ns, ...] (its floor tile is its first own tile)
+  const int n_own = (P.nt - c + P.ns - 1) / P.ns;
+  const int m = active ? n_own + (D.R.resid ? 1 : 0) : 0;
+  int ft = c;
+  auto tile_of = [&](int i) { return D.R.resid ? (i == 0 ? ft : c + (i - 1) * P.ns) : c + i * P.ns; };
+  int issued = 0;                                   // thread 0: tiles whose copies are issued
+  auto issue = [&](int i) {      // thread 0: bulk copies of the i-th tile into its stage
+    issued = i + 1 > issued ? i + 1 : issued;
+    const int t = tile_of(i), s = i % kStages;
+    const int v0 = t * kPartTile;
+    const unsigned bytes = (unsigned)((min(P.V, v0 + kPartTile) - v0) * sizeof(T));
+    mbar_arrive_tx(&S.bar[s], drow ? 2 * bytes : bytes);
+    bulk_copy_g2s(S.tile[s][0], trow + v0, bytes, &S.bar[s]);
+    if (drow) bulk_copy_g2s(S.tile[s][1], drow + v0, bytes, &S.bar[s]);
+  };
+  __syncthreads();                                   // barriers initialised
+  // the CTA's own tiles do not depend on the floor tile: start them now
+  if (bulk && threadIdx.x == 0)
+    for (int i = D.R.resid ? 1 : 0; i < min(m, kStages); ++i) issue(i);
+  if (active && D.R.resid) {
+    const long long rt_i = (long long)b * 2 * k + n;
+    const RowStat rt = ldcg_stat(P.ws.row_stat + rt_i);
+    const RowStat rd = ldcg_stat(P.ws.row_stat + rt_i + k);
+    D.R.mt = rt.m;
+    D.R.lnSt = rt.lnS;
+    D.R.cdelta = -(rd.m - rt.m) * P.invT - (rd.lnS - rt.lnS);
+    const Partial* piece = P.ws.row_partial + rt_i * P.nt;
+    float bm = -CUDART_INF_F;
+    int bi = INT_MAX;
+    for (int t = threadIdx.x; t < P.nt; t += kThreads) {
+      const float pm = __ldcg(&piece[t].m);
+      if (pm > bm) { bm = pm; bi = t; }
+    }
+    block_argmax(bm, bi, sh);
+    ft = bi < P.nt ? bi : 0;
+    if (bulk && threadIdx.x == 0) issue(0);
+  }
+  uint32_t* queue = S.queue[threadIdx.x >> 5];
+
+  float floor = -CUDART_INF_F, best = -CUDART_INF_F;
+  int bidx = INT_MAX, bad = 0;
+  int i = 0;
+  for (; i < m; ++i) {
+    const int s = i % kStages;
+    const int t = tile_of(i);
+    const int v0 = t * kPartTile, v1 = min(P.V, v0 + kPartTile);
+    const unsigned pub = __ldcg(P.ws.samp_floor + b);
+    bool ok = true;
+    if (bulk) {
+      ok = mbar_wait_bounded(&S.bar[s], (unsigned)(i / kStages) & 1u);
+      if (!ok) s_timeout = 1;
+    } else {
+      for (int o = threadIdx.x; o < v1 - v0; o += kThreads) {
+        S.tile[s][0][o] = trow[v0 + o];
+        if (drow) S.tile[s][1][o] = drow[v0 + o];
+      }
+      __syncthreads();
+    }
+    const T* st = S.tile[s][0];
+    const T* sd = S.tile[s][1];
+    if (i == 0) {
+      // 1. the floor: each thread's candidate with the largest target logit
+      float ub = -CUDART_INF_F, ub_xd = 0.f;
+      int ub_i = INT_MAX;
+      if (ok) {
+#pragma unroll
+        for (int q = 0; q < kGroups; ++q) {
+          const int o = 4 * (q * kThreads + threadIdx.x);
+          if (o >= v1 - v0) continue;
+          const Raw4<T> gt = lds_raw4<T>(st + o);
+          Raw4<T> gd;
+          if (D.R.resid) gd = lds_raw4<T>(sd + o);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (o + e >= v1 - v0) continue;
+            const float x = raw_at<T>(gt, e);
+            const float xdv = D.R.resid ? raw_at<T>(gd, e) : 0.f;
+            float h;
+            if (bound_of(D, x, xdv, h) && x > ub) { ub = x; ub_i = v0 + o + e; ub_xd = xdv; }
+          }
+        }
+      }
+      float f = ub > -CUDART_INF_F ? exact_score(D.invT, D.R, ub, ub_xd, uniform_at(D.key, D.gb, D.j, ub_i))
+                                   : -CUDART_INF_F;
+      f = warp_max(f);
+      if ((threadIdx.x & 31) == 0) s_floor[threadIdx.x >> 5] = f;
+      __syncthreads();
+      floor = from_ordered(pub);
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) floor = fmaxf(floor, s_floor[w]);
+      if (threadIdx.x == 0 && floor > -CUDART_INF_F) atomicMax(P.ws.samp_floor + b, ordered_bits(floor));
+    } else {
+      floor = fmaxf(floor, from_ordered(pub));
+    }
+    // 2. score the tile (the residual's floor tile is only the floor's)
+    if (ok && !(i == 0 && D.R.resid)) {
+      const float floor_in = floor;
+      score_tile<T>(D, v0, v1, st, sd, queue, floor, best, bidx, bad);
+      if (floor > floor_in) atomicMax(P.ws.samp_floor + b, ordered_bits(floor));
+    }
+    __syncthreads();                                 // the stage is free again
+    if (s_timeout) break;
+    if (bulk && threadIdx.x == 0 && i + kStages < m) {
+      fence_proxy_async_smem();
+      issue(i + kStages);
+    }
+  }
+  if (s_timeout && bulk) {
+    // leave no bulk copy in flight into this CTA's shared memory: wait (bounded)
+    // for every tile issued but not consumed, oldest first
+    if (threadIdx.x == 0)
+      for (int x = i; x < issued; ++x) mbar_wait_bounded(&S.bar[x % kStages], (unsigned)(x / kStages) & 1u);
+    __syncthreads();
+  }
+
+  // 3. partials and the merge
+  block_argmax_flag(best, bidx, bad, sh);
+  if (threadIdx.x == 0) {
+    // index -2 marks a tile that timed out
+    P.ws.samp_partial[(size_t)b * P.ns + c] =
+        make_float2(bad ? CUDART_NAN_F : best, __int_as_float(s_timeout ? -2 : bidx));
     __threadfence();
-    const unsigned old = atomicAdd(P.ws.samp_cnt + b, 1u);
-    s_last = old + 1 == (unsigned)P.nt2;
-    if (s_last) P.ws.samp_cnt[b] = 0;
+    s_last = atomicAdd(P.ws.samp_cnt + b, 1u) + 1 == (unsigned)P.ns;
+    if (s_last) {
+      P.ws.samp_cnt[b] = 0;
+      P.ws.samp_floor[b] = 0;
+    }
   }
   __syncthreads();
   if (!s_last) return;
+
   __threadfence();
   best = -CUDART_INF_F;
   bidx = INT_MAX;
   bad = 0;
-  for (int tt = threadIdx.x; tt < P.nt2; tt += kThreads) {
-    const float2 p = __ldcg(reinterpret_cast<const float2*>(P.ws.samp_partial) + (size_t)b * P.nt2 + tt);
-    if (p.x != p.x) { bad = 1; continue; }
+  int timed_out = 0;
+  for (int q = threadIdx.x; q < P.ns; q += kThreads) {
+    const float2 p = __ldcg(P.ws.samp_partial + (size_t)b * P.ns + q);
     const int pi = __float_as_int(p.y);
+    if (pi == -2) { timed_out = 1; continue; }
+    if (p.x != p.x) { bad = 1; continue; }
     if (beats(p.x, pi, best, bidx)) { best = p.x; bidx = pi; }
   }
-  bad = block_or(bad, sh);
-  block_argmax(best, bidx, sh);
-  int st = ss.status;
-  if (st == SPEC_OK && n == k && (bad || !(best > -CUDART_INF_F))) st = SPEC_ERR_NONFINITE;
-  if (st == SPEC_OK && n < k && bidx == INT_MAX) {
+  block_argmax_flag(best, bidx, bad, sh);
+  timed_out = __syncthreads_or(timed_out);
+  int st = status;
+  if (st == SPEC_OK && timed_out) st = SPEC_ERR_TIMEOUT;
+  if (st == SPEC_OK && !D.R.resid && (bad || !(best > -CUDART_INF_F))) st = SPEC_ERR_NONFINITE;
+  if (st == SPEC_OK && D.R.resid && bidx == INT_MAX) {
     // empty residual in fp32: draw from p_n itself with the same noise
-    const T* trow = (const T*)P.target + ((size_t)b * (k + 1) + n) * P.V;
+    const T* row = (const T*)P.target + ((size_t)b * (k + 1) + n) * P.V;
     best = -CUDART_INF_F;
     for (int g = threadIdx.x; 4 * g < P.V; g += kThreads) {
-      const uint4 w = gumbel_words(P.key, P.b0 + (uint32_t)b, n, (uint32_t)g);
+      const uint4 w = gumbel_words(P.key, D.gb, n, (uint32_t)g);
       const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
       for (int e = 0; e < 4 && 4 * g + e < P.V; ++e) {
         const int v = 4 * g + e;
-        const float sc = load_elem<T>(trow, v) * P.invT + gumbel_of(uniform_of(ws[e]));
+        const float sc = load_elem<T>(row, v) * P.invT + gumbel_of(uniform_of(ws[e]));
         if (beats(sc, v, best, bidx)) { best = sc; bidx = v; }
       }
     }
@@ -639,9 +999,9 @@ __global__ void __launch_bounds__(kThreads) sample_pass_kernel(const Params P) {
 // -------------------------------------------------------------- randomness ---
 __global__ void random_kernel(uint2 key, int b, int j, int V, float* gu, float* gg, float* au) {
   const int g = blockIdx.x * blockDim.x + threadIdx.x;
-  if (g == 0 && au) au[0] = accept_uniform(key, b, j);
+  if (g == 0 && au) au[0] = accept_uniform(key, (uint32_t)b, j);
   if (4 * g >= V) return;
-  const uint4 w = gumbel_words(key, b, j, (uint32_t)g);
+  const uint4 w = gumbel_words(key, (uint32_t)b, j, (uint32_t)g);
   const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
   for (int e = 0; e < 4 && 4 * g + e < V; ++e) {
     const float u = uniform_of(ws[e]);
@@ -653,8 +1013,8 @@ __global__ void random_kernel(uint2 key, int b, int j, int V, float* gu, float* 
 // --------------------------------------------------------------- host side ---
 
 struct Layout {
-  size_t row_partial, row_cnt, row_stat, seq_cnt, seq, samp_partial, samp_cnt, total;
-  int nt, nt2;
+  size_t row_partial, row_cnt, row_stat, seq_cnt, seq, samp_partial, samp_cnt, samp_floor, total;
+  int nt;
   long long rmax;
 };
 
@@ -662,8 +1022,7 @@ static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 static bool make_layout(int B, int k, int V, Layout& L) {
   if (B <= 0 || k <= 0 || V <= 0) return false;
-  L.nt = (V + kTile - 1) / kTile;
-  L.nt2 = (V + kSampleTile - 1) / kSampleTile;
+  L.nt = (V + kPartTile - 1) / kPartTile;
   L.rmax = (long long)B * (long long)(2 * k > k + 1 ? 2 * k : k + 1);
   size_t off = 0;
   auto take = [&](size_t bytes) { const size_t o = off; off = align_up(off + bytes, 256); return o; };
@@ -672,36 +1031,25 @@ static bool make_layout(int B, int k, int V, Layout& L) {
   L.row_stat = take((size_t)L.rmax * sizeof(RowStat));
   L.seq_cnt = take((size_t)B * sizeof(unsigned));
   L.seq = take((size_t)B * sizeof(SeqState));
-  L.samp_partial = take((size_t)B * L.nt2 * sizeof(Partial));
+  L.samp_partial = take((size_t)B * L.nt * sizeof(float2));
   L.samp_cnt = take((size_t)B * sizeof(unsigned));
+  L.samp_floor = take((size_t)B * sizeof(unsigned));
   L.total = off;
   return true;
 }
 
 static Workspace bind(void* base, const Layout& L) {
   char* p = static_cast<char*>(base);
-  return Workspace{reinterpret_cast<Partial*>(p + L.row_partial), reinterpret_cast<unsigned*>(p + L.row_cnt),
-                   reinterpret_cast<RowStat*>(p + L.row_stat),    reinterpret_cast<unsigned*>(p + L.seq_cnt),
-                   reinterpret_cast<SeqState*>(p + L.seq),        reinterpret_cast<Partial*>(p + L.samp_partial),
-                   reinterpret_cast<unsigned*>(p + L.samp_cnt)};
-}
-
-// Resident CTAs of a kernel on the current device, cached per (device, kernel).
-static int resident_ctas(const void* fn) {
-  static std::mutex mu;
-  static struct Entry { int dev; const void* fn; int ctas; } cache[64];
-  static int used = 0;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  std::lock_guard<std::mutex> lock(mu);
-  for (int i = 0; i < used; ++i)
-    if (cache[i].dev == dev && cache[i].fn == fn) return cache[i].ctas;
-  int sms = 0, per_sm = 0;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, 0) != cudaSuccess) return 0;
-  const int ctas = sms * (per_sm > 0 ? per_sm : 1);
-  if (used < 64) cache[used++] = Entry{dev, fn, ctas};
-  return ctas;
+  Workspace w;
+  w.row_partial = reinterpret_cast<Partial*>(p + L.row_partial);
+  w.row_cnt = reinterpret_cast<unsigned*>(p + L.row_cnt);
+  w.row_stat = reinterpret_cast<RowStat*>(p + L.row_stat);
+  w.seq_cnt = reinterpret_cast<unsigned*>(p + L.seq_cnt);
+  w.seq = reinterpret_cast<SeqState*>(p + L.seq);
+  w.samp_partial = reinterpret_cast<float2*>(p + L.samp_partial);
+  w.samp_cnt = reinterpret_cast<unsigned*>(p + L.samp_cnt);
+  w.samp_floor = reinterpret_cast<unsigned*>(p + L.samp_floor);
+  return w;
 }
 
 static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -728,28 +1076,67 @@ static int prepare_workspace(void* ws, const Layout& L, int B, int k, int V, cud
   return SPEC_OK;
 }
 
+// Resident CTAs of a kernel with `smem` bytes of dynamic shared memory on the
+// current device, cached per (device, kernel).
+static int resident_ctas(const void* fn, size_t smem = 0) {
+  static std::mutex mu;
+  static struct Entry { int dev; const void* fn; int ctas; } cache[64];
+  static int used = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i)
+    if (cache[i].dev == dev && cache[i].fn == fn) return cache[i].ctas;
+  int sms = 0, per_sm = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem) != cudaSuccess) return 0;
+  const int ctas = sms * (per_sm > 0 ? per_sm : 1);
+  if (used < 64) cache[used++] = Entry{dev, fn, ctas};
+  return ctas;
+}
+
 template <typename T, int kMode>
-static int launch_row_pass(const Params& P, cudaStream_t stream) {
-  const void* fn = reinterpret_cast<const void*>(&row_pass_kernel<T, kMode>);
-  const int ctas = resident_ctas(fn);
+static int launch(Params& P, cudaStream_t stream, const spec_verify_aux* aux) {
+  auto rec = [&](int i) {
+    return (aux && aux->events[i]) ? cudaEventRecord(static_cast<cudaEvent_t>(aux->events[i]), stream)
+                                   : cudaSuccess;
+  };
+  const void* rp = reinterpret_cast<const void*>(&row_pass_kernel<T, kMode>);
+  const int ctas = resident_ctas(rp);
   if (ctas <= 0) return SPEC_ERR_CUDA;
   const long long items = P.R * P.nt;
   const int grid = (int)(items < ctas ? items : ctas);
-  row_pass_kernel<T, kMode><<<grid, kThreads, 0, stream>>>(P);
-  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
-}
-
-template <typename T>
-static int launch_stochastic(const Params& P, cudaStream_t stream, const spec_verify_aux* aux) {
-  auto rec = [&](int i) {
-    return (aux && aux->events[i]) ? cudaEventRecord(static_cast<cudaEvent_t>(aux->events[i]), stream) : cudaSuccess;
-  };
   if (rec(0) != cudaSuccess) return SPEC_ERR_CUDA;
-  int rc = launch_row_pass<T, kStochastic>(P, stream);
-  if (rc != SPEC_OK) return rc;
-  if (rec(1) != cudaSuccess || rec(2) != cudaSuccess) return SPEC_ERR_CUDA;
-  sample_pass_kernel<T><<<P.B * P.nt2, kThreads, 0, stream>>>(P);
+  row_pass_kernel<T, kMode><<<grid, kThreads, 0, stream>>>(P);
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+  if (rec(1) != cudaSuccess) return SPEC_ERR_CUDA;
+  if constexpr (kMode == kStochastic) {
+    // as many CTAs per sequence as fill the GPU once, at most one per tile
+    const size_t smem = sizeof(SampleSmem<T>);
+    const int slots = resident_ctas(reinterpret_cast<const void*>(&sample_kernel<T>), smem);
+    if (slots <= 0) return SPEC_ERR_CUDA;
+    P.ns = slots / P.B;
+    P.ns = P.ns < 1 ? 1 : (P.ns > P.nt ? P.nt : P.ns);
+    if (rec(2) != cudaSuccess) return SPEC_ERR_CUDA;
+    // launched as a programmatic dependent of the row pass: its CTAs may start
+    // while the row pass drains and wait for its results in griddepcontrol.wait
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3((unsigned)(P.B * P.ns));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, sample_kernel<T>, P) != cudaSuccess) return SPEC_ERR_CUDA;
+  } else {
+    if (rec(2) != cudaSuccess) return SPEC_ERR_CUDA;
+  }
   return rec(3) == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
@@ -797,7 +1184,6 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, const in
   if (rc != SPEC_OK) return rc;
   if (!greedy && !aligned(draft_logits, dtype == SPEC_BF16 ? 2 : 4)) return SPEC_ERR_ALIGN;
   if (!aligned(draft_tokens, 4) || !aligned(out_tokens, 4) || !aligned(out_n_accepted, 4)) return SPEC_ERR_ALIGN;
-  if ((long long)B * L.nt2 > INT_MAX) return SPEC_ERR_UNSUPPORTED;
 
   Params P;
   std::memset(&P, 0, sizeof(P));
@@ -808,7 +1194,6 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, const in
   P.k = k;
   P.V = V;
   P.nt = L.nt;
-  P.nt2 = L.nt2;
   P.key = make_uint2((uint32_t)seed, (uint32_t)(seed >> 32));
   P.out_tokens = out_tokens;
   P.out_n = out_n_accepted;
@@ -825,20 +1210,14 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, const in
   if (greedy) {
     P.rows_per_seq = k + 1;
     P.R = (long long)B * (k + 1);
-    auto rec = [&](int i) {
-      return (aux && aux->events[i]) ? cudaEventRecord(static_cast<cudaEvent_t>(aux->events[i]), stream)
-                                     : cudaSuccess;
-    };
-    if (rec(0) != cudaSuccess) return SPEC_ERR_CUDA;
-    rc = dtype == SPEC_BF16 ? launch_row_pass<uint16_t, kGreedy>(P, stream) : launch_row_pass<float, kGreedy>(P, stream);
-    if (rc != SPEC_OK) return rc;
-    return rec(1) == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+    return dtype == SPEC_BF16 ? launch<uint16_t, kGreedy>(P, stream, aux) : launch<float, kGreedy>(P, stream, aux);
   }
   P.rows_per_seq = 2 * k;
   P.R = (long long)B * 2 * k;
   P.invT = 1.0f / temperature;
+  P.T = temperature;
   P.c = (float)(1.4426950408889634 / (double)temperature);
-  return dtype == SPEC_BF16 ? launch_stochastic<uint16_t>(P, stream, aux) : launch_stochastic<float>(P, stream, aux);
+  return dtype == SPEC_BF16 ? launch<uint16_t, kStochastic>(P, stream, aux) : launch<float, kStochastic>(P, stream, aux);
 }
 
 int spec_verify(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens, int B, int k, int V,
@@ -859,7 +1238,7 @@ int spec_verify_tree(const void* target_logits, const int32_t* node_tokens, cons
   if ((size_t)B * (size_t)(N + 1) > (size_t)INT_MAX) return SPEC_ERR_UNSUPPORTED;
   Layout L;
   make_layout(B, N, V, L);
-  const int rc = check_common(target_logits, B, V, dtype, workspace, L, workspace_bytes);
+  int rc = check_common(target_logits, B, V, dtype, workspace, L, workspace_bytes);
   if (rc != SPEC_OK) return rc;
   if (!aligned(node_tokens, 4) || !aligned(parents, 4) || !aligned(out_tokens, 4) || !aligned(out_n_accepted, 4))
     return SPEC_ERR_ALIGN;
@@ -872,7 +1251,6 @@ int spec_verify_tree(const void* target_logits, const int32_t* node_tokens, cons
   P.k = N;
   P.V = V;
   P.nt = L.nt;
-  P.nt2 = L.nt2;
   P.rows_per_seq = N + 1;
   P.R = (long long)B * (N + 1);
   P.out_tokens = out_tokens;
@@ -881,9 +1259,8 @@ int spec_verify_tree(const void* target_logits, const int32_t* node_tokens, cons
   P.status = status;
   P.ws = bind(workspace, L);
   cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
-  const int prc = prepare_workspace(workspace, L, B, N, V, stream);
-  if (prc != SPEC_OK) return prc;
-  return dtype == SPEC_BF16 ? launch_row_pass<uint16_t, kTree>(P, stream) : launch_row_pass<float, kTree>(P, stream);
+  if ((rc = prepare_workspace(workspace, L, B, N, V, stream)) != SPEC_OK) return rc;
+  return dtype == SPEC_BF16 ? launch<uint16_t, kTree>(P, stream, nullptr) : launch<float, kTree>(P, stream, nullptr);
 }
 
 int spec_random(uint64_t seed, int b, int j, int V, float* gumbel_u, float* gumbel_g, float* accept_u,

@@ -69,7 +69,7 @@ def test_noalloc_matches_spec_verify_on_consecutive_calls(abi):
 
 def test_noalloc_refuses_sizes_beyond_its_scratch(abi):
     sv, lib = abi
-    B, k, V = 1024, 8, 128256
+    B, k, V = 4096, 8, 128256
     assert sv.workspace_size(B, k, V) > 8 << 20
     dummy = ctypes.c_void_p(0x1000)                   # never touched: the call returns before any launch
     rc = lib.spec_verify_noalloc(dummy, dummy, dummy, B, k, V, sv.SPEC_BF16, 1.0, ctypes.c_uint64(0), dummy, dummy,
