@@ -80,6 +80,7 @@ enum spec_status {
 /* Limits of this build. */
 #define SPEC_MAX_K 1024        /* drafts per sequence (spec_verify)              */
 #define SPEC_MAX_TREE_N 4096   /* nodes per sequence (spec_verify_tree)          */
+#define SPEC_MAX_STOP 64       /* stop ids per call (spec_verify_aux.stop_ids)   */
 
 /* Bytes of device workspace for B sequences of k drafts (or N tree nodes) over
  * V ids.  Enough for spec_verify, spec_verify_ex and spec_verify_tree with the
@@ -126,6 +127,27 @@ typedef struct spec_verify_aux {
   uint32_t sequence_offset; /* global index of sequence 0 in the Philox counters: a batch  */
                        /*   split across devices draws the same numbers as the whole batch  */
                        /*   when each shard passes the index of its first sequence          */
+
+  /* ---- since ABI 1.1 (zero-initialise the struct: zero keeps each off) ---- */
+
+  float lenience;      /* stochastic: l >= 1 ("Cascade Speculative Drafting for Even Faster */
+                       /*   LLM Inference", "Asymmetric lenience"): accept when q <= l p,    */
+                       /*   otherwise keep with probability l p / q; the residual stays      */
+                       /*   norm(max(0, p - q)).  0 or 1 = the exact rule; any other value   */
+                       /*   below 1, or not finite, is SPEC_ERR_ARG.  l > 1 changes the      */
+                       /*   output law: the pages apply it only when a draft model reviews.  */
+  const int32_t* stop_ids; /* device [n_stop] or NULL: the committed tokens end at the first */
+                       /*   one that is a stop id ("Speculative Decoding: ...", "Constraints */
+                       /*   must be applied consistently"); the later ones become -1         */
+  int32_t n_stop;      /* 0..SPEC_MAX_STOP (n_stop > 0 with stop_ids NULL: SPEC_ERR_ARG)     */
+  int32_t* n_committed; /* device [B] or NULL: committed tokens per sequence after the stop  */
+                       /*   truncation (n_accepted + 1 without one); -1 for a bad sequence   */
+  uint8_t* match_mask; /* greedy (temperature 0) only, device [B][k] or NULL: 1 iff x_i is   */
+                       /*   the argmax of target row i ("Ouroboros: ...", Equation (10))     */
+  int32_t* n_match;    /* greedy only, device [B] or NULL: #Match = the mask's sum           */
+  int32_t* tail_runs;  /* greedy only, device [B] or NULL: maximal runs of matches after the */
+                       /*   first mismatch (the segments a phrase harvester keeps)           */
+                       /* Any of the three in stochastic mode: SPEC_ERR_ARG.                 */
 } spec_verify_aux;
 
 /* spec_verify plus the auxiliary outputs in `aux` (which may be NULL). */
@@ -200,6 +222,34 @@ int spec_random(uint64_t seed, int b, int j, int V, float* gumbel_u, float* gumb
 int spec_verify_noalloc(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
                         int B, int k, int V, int dtype, float temperature, uint64_t seed,
                         int32_t* out_tokens, int32_t* out_n_accepted, void* cuda_stream);
+
+/*
+ * spec_verify_guided -- greedy verification followed by a target-side guide
+ * ("Double: Breaking the Acceleration Limit via Double Retrieval Speculative
+ * Parallelism", "Multi-token Pre-verify" and D.2 "Proof of Lossless
+ * Acceleration", greedy decoding).
+ *
+ *   target_logits   device, [B][k+1][V] of dtype (as spec_verify, greedy)
+ *   draft_tokens    device, [B][k] int32
+ *   guide           device, [B][L] int32: the target-side token for each
+ *                   position 0..L-1; a negative entry ends the guide (may be
+ *                   NULL when L == 0)
+ *   out_tokens      device, [B][max(k+1, L)] int32
+ *   out_n_accepted  device, [B]: accepted drafts n
+ *   out_n_committed device, [B]: committed tokens
+ *   status          device, [B] or NULL
+ *
+ * Committed: x_0..x_{n-1} (the drafts that equal the target argmax of their
+ * row), the correction a*_n (the argmax of row n; the bonus when n = k), and,
+ * when guide[n] == a*_n, the guide's tokens guide[n+1], guide[n+2], ... up to
+ * its end: they follow the corrected target path.  Then -1.  A guide id >= V
+ * is SPEC_ERR_TOKEN for the sequence.  Workspace: spec_workspace_size(B, k,
+ * V, dtype).  Host errors as spec_verify (L < 0: SPEC_ERR_ARG).
+ */
+int spec_verify_guided(const void* target_logits, const int32_t* draft_tokens, const int32_t* guide,
+                       int B, int k, int L, int V, int dtype,
+                       int32_t* out_tokens, int32_t* out_n_accepted, int32_t* out_n_committed,
+                       int32_t* status, void* workspace, size_t workspace_bytes, void* cuda_stream);
 
 /* Human-readable name of a status code (static storage). */
 const char* spec_strerror(int status);

@@ -53,7 +53,7 @@ class _Replay:
         return self._next([(v, float(w[v])) for v in range(w.shape[0]) if w[v] > 0])
 
 
-def output_law(logp: np.ndarray, logq: np.ndarray, tokens):
+def output_law(logp: np.ndarray, logq: np.ndarray, tokens, lenience: float = 1.0):
     """Exact law of the committed-token tuple for fixed draft tokens."""
     law = defaultdict(float)
     stack = [[]]
@@ -61,7 +61,7 @@ def output_law(logp: np.ndarray, logq: np.ndarray, tokens):
         script = stack.pop()
         rp = _Replay(script)
         try:
-            out, _ = verify_sequence(logp, logq, tokens, rp.accept, rp.draw)
+            out, _ = verify_sequence(logp, logq, tokens, rp.accept, rp.draw, lenience=lenience)
         except _Branch as br:
             for choice, weight in br.options:
                 if weight > 0:
@@ -71,7 +71,7 @@ def output_law(logp: np.ndarray, logq: np.ndarray, tokens):
     return law
 
 
-def full_law(logp: np.ndarray, logq: np.ndarray):
+def full_law(logp: np.ndarray, logq: np.ndarray, lenience: float = 1.0):
     """Exact law of the committed tuple when the drafts themselves are drawn
     x_i ~ q_i independently (context-free rows)."""
     k, V = logq.shape
@@ -81,6 +81,6 @@ def full_law(logp: np.ndarray, logq: np.ndarray):
         w = float(np.prod([q[i, xs[i]] for i in range(k)]))
         if w == 0.0:
             continue
-        for out, pr in output_law(logp, logq, xs).items():
+        for out, pr in output_law(logp, logq, xs, lenience).items():
             law[out] += w * pr
     return law

@@ -62,7 +62,8 @@ def log_softmax(logits: np.ndarray, temperature: float):
 # The rule for one sequence, with its two sources of randomness as hooks.
 # ----------------------------------------------------------------------------
 
-def verify_sequence(logp: np.ndarray, logq: np.ndarray, tokens, accept: Callable, draw: Callable):
+def verify_sequence(logp: np.ndarray, logq: np.ndarray, tokens, accept: Callable, draw: Callable,
+                    lenience: float = 1.0):
     """One sequence of speculative verification.
 
     logp   (k+1, V) natural-log target probabilities (row k is the bonus row)
@@ -71,6 +72,10 @@ def verify_sequence(logp: np.ndarray, logq: np.ndarray, tokens, accept: Callable
     accept(i, ratio) -> bool     True with probability min(1, ratio)
     draw(j, logw, kind) -> int   one draw from the law proportional to exp(logw)
                                  (-inf entries excluded); kind names the draw
+    lenience l >= 1              "Cascade Speculative Drafting ...", "Asymmetric
+                                 lenience": accept when q <= l p, otherwise reject
+                                 with probability 1 - l p / q; the residual stays
+                                 norm(max(0, p - q)).  l = 1 is the exact rule.
 
     Returns (committed token list, number of accepted drafts n).
     """
@@ -80,7 +85,7 @@ def verify_sequence(logp: np.ndarray, logq: np.ndarray, tokens, accept: Callable
         x = int(tokens[i])
         p = float(np.exp(logp[i, x]))
         q = float(np.exp(logq[i, x]))
-        if q <= p or accept(i, p / q):
+        if q <= lenience * p or accept(i, lenience * p / q):
             out.append(x)
             continue
         # residual max(0, p - q), as a log weight: ln p + ln(1 - q/p) where p > q
@@ -127,17 +132,18 @@ def _philox_accept(seed: int, b: int):
     return accept
 
 
-def position_margins(seed: int, b: int, p_draft, q_draft, n: int, k: int, draw_gap: float) -> np.ndarray:
+def position_margins(seed: int, b: int, p_draft, q_draft, n: int, k: int, draw_gap: float,
+                     lenience: float = 1.0) -> np.ndarray:
     """Distance of each committed position's decision from its boundary.
 
-    Position i < n: |u_i - min(1, p/q)| of its accept decision.  Position n:
+    Position i < n: |u_i - min(1, l p/q)| of its accept decision.  Position n:
     the smaller of that distance for the rejecting decision (when n < k) and
     the Gumbel top-1 / top-2 gap of the draw.  A position whose margin is
     below the parity threshold may legitimately come out differently in fp32.
     """
     m = np.empty(n + 1)
     for i in range(min(n + 1, k)):
-        ratio = np.inf if q_draft[i] == 0 else p_draft[i] / q_draft[i]
+        ratio = np.inf if q_draft[i] == 0 else lenience * p_draft[i] / q_draft[i]
         m[i] = abs(philox.accept_uniform(seed, b, i) - min(1.0, ratio))
     m[n] = min(m[n], draw_gap) if n < k else draw_gap
     return m
@@ -162,11 +168,12 @@ class StochasticResult:
 
 
 def verify_stochastic(target, draft, tokens, dtype: str, temperature: float, seed: int,
-                      seq_offset: int = 0) -> StochasticResult:
+                      seq_offset: int = 0, lenience: float = 1.0) -> StochasticResult:
     """Stochastic verification of B sequences (oracle).
 
     target [B][k+1][V], draft [B][k][V] stored logits; tokens [B][k].  Sequence b
-    draws the randomness of global sequence index seq_offset + b.
+    draws the randomness of global sequence index seq_offset + b.  lenience as in
+    verify_sequence.
     """
     t = decode_logits(target, dtype)
     d = decode_logits(draft, dtype)
@@ -198,14 +205,14 @@ def verify_stochastic(target, draft, tokens, dtype: str, temperature: float, see
         q_d[b] = np.exp(logq[np.arange(k), tokens[b]])
         gb = seq_offset + b
         seq, n = verify_sequence(logp, logq, tokens[b], _philox_accept(seed, gb),
-                                 _gumbel_draw(seed, gb, trace))
+                                 _gumbel_draw(seed, gb, trace), lenience=lenience)
         if n == k and _bad_rows(t[b, k:k + 1]):
             status[b] = STATUS_NONFINITE
             continue
         out[b, :len(seq)] = seq
         n_acc[b] = n
         empty[b] = trace.empty_residual
-        margins[b] = position_margins(seed, gb, p_d[b], q_d[b], n, k, trace.draw_gap)
+        margins[b] = position_margins(seed, gb, p_d[b], q_d[b], n, k, trace.draw_gap, lenience)
     return StochasticResult(out, n_acc, p_d, q_d, lse_t, lse_d, status, margins, empty)
 
 

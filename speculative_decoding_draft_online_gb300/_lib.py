@@ -31,9 +31,15 @@ class SpecError(RuntimeError):
 
 
 class _Aux(ctypes.Structure):
+    """spec_verify_aux of ABI 1.1."""
     _fields_ = [("p_draft", ctypes.c_void_p), ("q_draft", ctypes.c_void_p), ("lse", ctypes.c_void_p),
                 ("status", ctypes.c_void_p), ("events", ctypes.c_void_p * 4),
-                ("sequence_offset", ctypes.c_uint32)]
+                ("sequence_offset", ctypes.c_uint32), ("lenience", ctypes.c_float),
+                ("stop_ids", ctypes.c_void_p), ("n_stop", ctypes.c_int32), ("n_committed", ctypes.c_void_p),
+                ("match_mask", ctypes.c_void_p), ("n_match", ctypes.c_void_p), ("tail_runs", ctypes.c_void_p)]
+
+
+ABI_MIN = (1 << 16) | 1
 
 
 def _load():
@@ -53,12 +59,16 @@ def _load():
     L.spec_verify_ex.restype = i32
     L.spec_verify_tree.argtypes = [vp, vp, vp, i32, i32, i32, i32, f32, vp, vp, vp, vp, vp, sz, vp]
     L.spec_verify_tree.restype = i32
+    L.spec_verify_guided.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
+    L.spec_verify_guided.restype = i32
     L.spec_random.argtypes = [u64, i32, i32, i32, vp, vp, vp, vp]
     L.spec_random.restype = i32
     L.spec_strerror.argtypes = [i32]
     L.spec_strerror.restype = ctypes.c_char_p
     L.spec_abi_version.argtypes = []
     L.spec_abi_version.restype = i32
+    if L.spec_abi_version() < ABI_MIN or (L.spec_abi_version() >> 16) != (ABI_MIN >> 16):
+        raise ImportError(f"{LIB_PATH} has ABI {L.spec_abi_version():#x}, this binding needs {ABI_MIN:#x}")
     return L
 
 
@@ -122,14 +132,21 @@ def _check(t: torch.Tensor, name: str, shape, dtype=None):
 
 def verify_ex(target: torch.Tensor, draft: Optional[torch.Tensor], tokens: torch.Tensor, temperature: float,
               seed: int = 0, *, out_tokens=None, out_n=None, ws=None, stream=None, aux: bool = False,
-              events=None, sequence_offset: int = 0):
+              events=None, sequence_offset: int = 0, lenience: float = 1.0,
+              stop_ids: Optional[torch.Tensor] = None, committed: bool = False, match: bool = False):
     """spec_verify_ex on torch tensors.
 
     target [B][k+1][V] and draft [B][k][V] (bf16 or fp32, same dtype), tokens
     [B][k] int32.  temperature == 0 selects greedy verification (draft may be
-    None).  Returns (out_tokens [B][k+1] int32, n_accepted [B] int32) and, with
-    aux=True, a dict of p_draft, q_draft, lse and status.  sequence_offset is
-    the global index of sequence 0 when the batch is a shard of a larger one.
+    None).  Returns (out_tokens [B][k+1] int32, n_accepted [B] int32), plus a
+    dict when any of these is asked for:
+      aux=True        p_draft, q_draft, lse, status
+      committed=True  n_committed (after truncation at stop_ids)
+      match=True      (greedy) match_mask [B][k] uint8, n_match, tail_runs
+    sequence_offset is the global index of sequence 0 when the batch is a
+    shard of a larger one; lenience >= 1 loosens the stochastic accept test;
+    stop_ids is an int32 CUDA tensor of stop ids (the committed tokens end at
+    the first one).
     """
     B, k1, V = target.shape
     k = k1 - 1
@@ -141,6 +158,8 @@ def verify_ex(target: torch.Tensor, draft: Optional[torch.Tensor], tokens: torch
             raise ValueError("stochastic verification needs draft logits")
         _check(draft, "draft", (B, k, V), target.dtype)
     _check(tokens, "tokens", (B, k), torch.int32)
+    if stop_ids is not None:
+        _check(stop_ids, "stop_ids", (stop_ids.numel(),), torch.int32)
     if out_tokens is None:
         out_tokens = torch.empty((B, k + 1), dtype=torch.int32, device=dev)
     if out_n is None:
@@ -149,16 +168,29 @@ def verify_ex(target: torch.Tensor, draft: Optional[torch.Tensor], tokens: torch
         ws = workspace(B, k, V, code, dev, stream)
     extra = {}
     a = None
-    if aux or events is not None or sequence_offset:
+    if (aux or events is not None or sequence_offset or lenience != 1.0 or stop_ids is not None or committed
+            or match):
         a = _Aux()
         a.sequence_offset = int(sequence_offset)
+        a.lenience = float(lenience)
         if aux:
-            extra = dict(p_draft=torch.zeros((B, k), dtype=torch.float32, device=dev),
+            extra.update(p_draft=torch.zeros((B, k), dtype=torch.float32, device=dev),
                          q_draft=torch.zeros((B, k), dtype=torch.float32, device=dev),
                          lse=torch.zeros((B, 2 * k), dtype=torch.float32, device=dev),
                          status=torch.zeros((B,), dtype=torch.int32, device=dev))
             a.p_draft, a.q_draft = extra["p_draft"].data_ptr(), extra["q_draft"].data_ptr()
             a.lse, a.status = extra["lse"].data_ptr(), extra["status"].data_ptr()
+        if stop_ids is not None and stop_ids.numel() > 0:
+            a.stop_ids, a.n_stop = stop_ids.data_ptr(), int(stop_ids.numel())
+        if committed:
+            extra["n_committed"] = torch.empty((B,), dtype=torch.int32, device=dev)
+            a.n_committed = extra["n_committed"].data_ptr()
+        if match:
+            extra.update(match_mask=torch.empty((B, k), dtype=torch.uint8, device=dev),
+                         n_match=torch.empty((B,), dtype=torch.int32, device=dev),
+                         tail_runs=torch.empty((B,), dtype=torch.int32, device=dev))
+            a.match_mask, a.n_match = extra["match_mask"].data_ptr(), extra["n_match"].data_ptr()
+            a.tail_runs = extra["tail_runs"].data_ptr()
         if events is not None:
             for i, e in enumerate(events[:4]):
                 a.events[i] = None if e is None else e.cuda_event
@@ -168,7 +200,7 @@ def verify_ex(target: torch.Tensor, draft: Optional[torch.Tensor], tokens: torch
     rc = lib.spec_verify_ex(*args, ctypes.byref(a) if a is not None else None)
     if rc != SPEC_OK:
         raise SpecError(rc, "spec_verify_ex")
-    if aux:
+    if extra:
         return out_tokens, out_n, extra
     return out_tokens, out_n
 
@@ -201,6 +233,36 @@ def verify_tree(target: torch.Tensor, node_tokens: torch.Tensor, parents: torch.
     if rc != SPEC_OK:
         raise SpecError(rc, "spec_verify_tree")
     return out, n, leaf, status
+
+
+def verify_guided(target: torch.Tensor, tokens: torch.Tensor, guide: torch.Tensor, *, ws=None, stream=None):
+    """spec_verify_guided (greedy verification, then the target-side guide).
+
+    target [B][k+1][V], tokens [B][k] int32, guide [B][L] int32 (negative =
+    past its end).  Returns (out_tokens [B][max(k+1, L)], n_accepted [B],
+    n_committed [B], status [B]).
+    """
+    B, k1, V = target.shape
+    k = k1 - 1
+    L = guide.shape[1] if guide.dim() == 2 else 0
+    code = dtype_code(target)
+    dev = target.device
+    _check(target, "target", (B, k + 1, V))
+    _check(tokens, "tokens", (B, k), torch.int32)
+    _check(guide, "guide", (B, L), torch.int32)
+    W = max(k + 1, L)
+    out = torch.empty((B, W), dtype=torch.int32, device=dev)
+    n = torch.empty((B,), dtype=torch.int32, device=dev)
+    nc = torch.empty((B,), dtype=torch.int32, device=dev)
+    status = torch.empty((B,), dtype=torch.int32, device=dev)
+    if ws is None:
+        ws = workspace(B, k, V, code, dev, stream)
+    rc = lib.spec_verify_guided(_ptr(target), _ptr(tokens), _ptr(guide) if L > 0 else None, B, k, L, V, code,
+                                _ptr(out), _ptr(n), _ptr(nc), _ptr(status), _ptr(ws), ws.numel(),
+                                _stream_ptr(stream, dev))
+    if rc != SPEC_OK:
+        raise SpecError(rc, "spec_verify_guided")
+    return out, n, nc, status
 
 
 def random_stream(seed: int, b: int, j: int, V: int, device="cuda", stream=None):

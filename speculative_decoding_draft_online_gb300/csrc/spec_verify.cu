@@ -111,6 +111,17 @@ struct Params {
   float* p_draft;
   float* q_draft;
   float* lse;
+  int out_w;                   // out_tokens row width
+  float lenience;              // l >= 1 (stochastic); 1 is the exact rule
+  float ln_lenience;           // ln l
+  const int32_t* stop_ids;     // [n_stop]: the committed tokens end at the first one
+  int n_stop;
+  int32_t* n_committed;        // [B] or null
+  uint8_t* match_mask;         // greedy: [B][k] or null
+  int32_t* n_match;            // greedy: [B] or null
+  int32_t* tail_runs;          // greedy: [B] or null
+  const int32_t* guide;        // guided greedy: [B][L] or null
+  int L;
   Workspace ws;
 };
 
@@ -340,7 +351,8 @@ __device__ void accept_scan(const Params& P, int b) {
         const float lp = (xt - rt.m) * P.invT - rt.lnS;   // ln p_i(x_i)
         const float lq = (xd - rd.m) * P.invT - rd.lnS;   // ln q_i(x_i)
         const float u = accept_uniform(P.key, P.b0 + (uint32_t)b, i);
-        acc = (lq <= lp) || (u < expf(lp - lq));
+        // "Asymmetric lenience": keep when q <= l p, else with probability l p / q
+        acc = (lq <= lp + P.ln_lenience) || (u < P.lenience * expf(lp - lq));
         if (P.p_draft) P.p_draft[(size_t)b * k + i] = expf(lp);
         if (P.q_draft) P.q_draft[(size_t)b * k + i] = expf(lq);
       }
@@ -360,7 +372,44 @@ __device__ void accept_scan(const Params& P, int b) {
   }
 }
 
-// Greedy match: n = first i with x_i != argmax_i.
+// Write one sequence's committed tokens with one warp.  token(i) is the i-th
+// committed token, or -1 past the last; the row ends after the first token
+// that is a stop id ("Speculative Decoding: ...", "Constraints must be
+// applied consistently": nothing after an end-of-sequence token is kept).
+// Returns the committed count.
+template <class F>
+__device__ int write_committed(const Params& P, int32_t* out, int width, F token) {
+  const int lane = threadIdx.x & 31;
+  int cut = INT_MAX;                                 // position of the first stop token
+  if (P.n_stop > 0) {
+    for (int base = 0; base < width && cut == INT_MAX; base += 32) {
+      const int i = base + lane;
+      bool stop = false;
+      if (i < width) {
+        const int v = token(i);
+        if (v >= 0)
+          for (int s = 0; s < P.n_stop; ++s) stop |= v == __ldg(P.stop_ids + s);
+      }
+      const unsigned m = __ballot_sync(0xffffffffu, stop);
+      if (m) cut = base + __ffs(m) - 1;
+    }
+  }
+  int count = 0;
+  for (int base = 0; base < width; base += 32) {
+    const int i = base + lane;
+    int v = -1;
+    if (i < width && i <= cut) v = token(i);
+    if (i < width) out[i] = v;
+    count += __popc(__ballot_sync(0xffffffffu, v >= 0));
+  }
+  return count;
+}
+
+// Greedy match: n = first i with x_i != argmax_i.  With a guide ("Double: ...",
+// "Multi-token Pre-verify"), the correction is followed by the guide's tokens
+// when the guide agrees with it.  Optionally the per-position matches
+// ("Ouroboros: ...", Equation (10)), their count and the runs of matches after
+// the first mismatch.
 __device__ void greedy_match(const Params& P, int b) {
   const int lane = threadIdx.x & 31;
   const int k = P.k;
@@ -384,15 +433,56 @@ __device__ void greedy_match(const Params& P, int b) {
     const unsigned mm = __ballot_sync(0xffffffffu, mism);
     if (n == k && mm) n = base + __ffs(mm) - 1;
   }
-  const int st = tok_bad ? SPEC_ERR_TOKEN : nf_bad ? SPEC_ERR_NONFINITE : SPEC_OK;
+  // the guide: ids must be in range; it continues the corrected path only if
+  // it agrees with the correction, and it ends at its first negative entry
   const int an = ldcg_stat(P.ws.row_stat + rbase + n).arg;
-  for (int i = lane; i <= k; i += 32) {
-    int v = -1;
-    if (st == SPEC_OK) v = i < n ? P.tokens[(size_t)b * k + i] : (i == n ? an : -1);
-    P.out_tokens[(size_t)b * (k + 1) + i] = v;
+  const int32_t* g = P.guide ? P.guide + (size_t)b * P.L : nullptr;
+  int gend = n + 1;
+  if (g) {
+    unsigned gbad = 0;
+    int first_neg = P.L;
+    for (int base = 0; base < P.L; base += 32) {
+      const int i = base + lane;
+      const int v = i < P.L ? g[i] : 0;
+      gbad |= __ballot_sync(0xffffffffu, v >= P.V);
+      const unsigned neg = __ballot_sync(0xffffffffu, i < P.L && i > n && v < 0);
+      if (neg && first_neg == P.L) first_neg = base + __ffs(neg) - 1;
+    }
+    tok_bad |= gbad;
+    if (n < P.L && g[n] == an) gend = first_neg;
+  }
+  const int st = tok_bad ? SPEC_ERR_TOKEN : nf_bad ? SPEC_ERR_NONFINITE : SPEC_OK;
+  int32_t* out = P.out_tokens + (size_t)b * P.out_w;
+  const int32_t* x = P.tokens + (size_t)b * k;
+  const int committed = write_committed(P, out, P.out_w, [&](int i) -> int {
+    if (st != SPEC_OK) return -1;
+    if (i < n) return x[i];
+    if (i == n) return an;
+    return i < gend ? g[i] : -1;
+  });
+  if (P.match_mask || P.n_match || P.tail_runs) {
+    int n_match = 0, runs = 0;
+    unsigned carry = 1;                              // position -1 counts as a match
+    for (int base = 0; base < k; base += 32) {
+      const int i = base + lane;
+      bool hit = false;
+      if (i < k && st == SPEC_OK) hit = x[i] == ldcg_stat(P.ws.row_stat + rbase + i).arg;
+      if (i < k && P.match_mask) P.match_mask[(size_t)b * k + i] = hit ? 1 : 0;
+      const unsigned hits = __ballot_sync(0xffffffffu, hit);
+      const unsigned starts = hits & ~((hits << 1) | carry);
+      const unsigned after = __ballot_sync(0xffffffffu, i > n);
+      n_match += __popc(hits);
+      runs += __popc(starts & after);
+      carry = hits >> 31;
+    }
+    if (lane == 0) {
+      if (P.n_match) P.n_match[b] = st == SPEC_OK ? n_match : -1;
+      if (P.tail_runs) P.tail_runs[b] = st == SPEC_OK ? runs : -1;
+    }
   }
   if (lane == 0) {
     P.out_n[b] = st == SPEC_OK ? n : -1;
+    if (P.n_committed) P.n_committed[b] = st == SPEC_OK ? committed : -1;
     if (P.status) P.status[b] = st;
   }
 }
@@ -984,14 +1074,16 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const Params P) {
     }
     block_argmax(best, bidx, sh);
   }
-  int32_t* out = P.out_tokens + (size_t)b * (k + 1);
-  for (int i = threadIdx.x; i <= k; i += kThreads) {
-    int v = -1;
-    if (st == SPEC_OK) v = i < n ? P.tokens[(size_t)b * k + i] : (i == n ? bidx : -1);
-    out[i] = v;
-  }
+  if (threadIdx.x >= 32) return;
+  int32_t* out = P.out_tokens + (size_t)b * P.out_w;
+  const int32_t* x = P.tokens + (size_t)b * k;
+  const int committed = write_committed(P, out, P.out_w, [&](int i) -> int {
+    if (st != SPEC_OK) return -1;
+    return i < n ? x[i] : (i == n ? bidx : -1);
+  });
   if (threadIdx.x == 0) {
     P.out_n[b] = st == SPEC_OK ? n : -1;
+    if (P.n_committed) P.n_committed[b] = st == SPEC_OK ? committed : -1;
     if (P.status) P.status[b] = st;
   }
 }
@@ -1185,6 +1277,20 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, const in
   if (!greedy && !aligned(draft_logits, dtype == SPEC_BF16 ? 2 : 4)) return SPEC_ERR_ALIGN;
   if (!aligned(draft_tokens, 4) || !aligned(out_tokens, 4) || !aligned(out_n_accepted, 4)) return SPEC_ERR_ALIGN;
 
+  float lenience = 1.f;
+  if (aux) {
+    if (aux->lenience != 0.f) {
+      if (!(aux->lenience >= 1.f) || !std::isfinite(aux->lenience)) return SPEC_ERR_ARG;
+      lenience = aux->lenience;
+    }
+    if (aux->n_stop < 0 || (aux->n_stop > 0 && !aux->stop_ids)) return SPEC_ERR_ARG;
+    if (aux->n_stop > SPEC_MAX_STOP) return SPEC_ERR_UNSUPPORTED;
+    if (!greedy && (aux->match_mask || aux->n_match || aux->tail_runs)) return SPEC_ERR_ARG;
+    if ((aux->stop_ids && !aligned(aux->stop_ids, 4)) || (aux->n_committed && !aligned(aux->n_committed, 4)) ||
+        (aux->n_match && !aligned(aux->n_match, 4)) || (aux->tail_runs && !aligned(aux->tail_runs, 4)))
+      return SPEC_ERR_ALIGN;
+  }
+
   Params P;
   std::memset(&P, 0, sizeof(P));
   P.target = target_logits;
@@ -1197,6 +1303,9 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, const in
   P.key = make_uint2((uint32_t)seed, (uint32_t)(seed >> 32));
   P.out_tokens = out_tokens;
   P.out_n = out_n_accepted;
+  P.out_w = k + 1;
+  P.lenience = lenience;
+  P.ln_lenience = (float)std::log((double)lenience);
   P.ws = bind(workspace, L);
   if (aux) {
     P.status = aux->status;
@@ -1204,6 +1313,12 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, const in
     P.q_draft = aux->q_draft;
     P.lse = aux->lse;
     P.b0 = aux->sequence_offset;
+    P.stop_ids = aux->n_stop > 0 ? aux->stop_ids : nullptr;
+    P.n_stop = aux->n_stop > 0 ? aux->n_stop : 0;
+    P.n_committed = aux->n_committed;
+    P.match_mask = aux->match_mask;
+    P.n_match = aux->n_match;
+    P.tail_runs = aux->tail_runs;
   }
   cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
   if ((rc = prepare_workspace(workspace, L, B, k, V, stream)) != SPEC_OK) return rc;
@@ -1253,6 +1368,8 @@ int spec_verify_tree(const void* target_logits, const int32_t* node_tokens, cons
   P.nt = L.nt;
   P.rows_per_seq = N + 1;
   P.R = (long long)B * (N + 1);
+  P.out_w = N + 1;
+  P.lenience = 1.f;
   P.out_tokens = out_tokens;
   P.out_n = out_n_accepted;
   P.out_leaf = out_leaf;
@@ -1261,6 +1378,46 @@ int spec_verify_tree(const void* target_logits, const int32_t* node_tokens, cons
   cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
   if ((rc = prepare_workspace(workspace, L, B, N, V, stream)) != SPEC_OK) return rc;
   return dtype == SPEC_BF16 ? launch<uint16_t, kTree>(P, stream, nullptr) : launch<float, kTree>(P, stream, nullptr);
+}
+
+int spec_verify_guided(const void* target_logits, const int32_t* draft_tokens, const int32_t* guide, int B, int k,
+                       int L, int V, int dtype, int32_t* out_tokens, int32_t* out_n_accepted,
+                       int32_t* out_n_committed, int32_t* status, void* workspace, size_t workspace_bytes,
+                       void* cuda_stream) {
+  if (k <= 0 || B <= 0 || V <= 0 || L < 0) return SPEC_ERR_ARG;
+  if (k > SPEC_MAX_K) return SPEC_ERR_UNSUPPORTED;
+  if (!draft_tokens || !out_tokens || !out_n_accepted || !out_n_committed || (L > 0 && !guide)) return SPEC_ERR_ARG;
+  const int W = L > k + 1 ? L : k + 1;
+  if ((size_t)B * (size_t)W > (size_t)INT_MAX) return SPEC_ERR_UNSUPPORTED;
+  Layout Lw;
+  make_layout(B, k, V, Lw);
+  int rc = check_common(target_logits, B, V, dtype, workspace, Lw, workspace_bytes);
+  if (rc != SPEC_OK) return rc;
+  if (!aligned(draft_tokens, 4) || !aligned(out_tokens, 4) || !aligned(out_n_accepted, 4) ||
+      !aligned(out_n_committed, 4) || (guide && !aligned(guide, 4)) || (status && !aligned(status, 4)))
+    return SPEC_ERR_ALIGN;
+  Params P;
+  std::memset(&P, 0, sizeof(P));
+  P.target = target_logits;
+  P.tokens = draft_tokens;
+  P.B = B;
+  P.k = k;
+  P.V = V;
+  P.nt = Lw.nt;
+  P.out_tokens = out_tokens;
+  P.out_n = out_n_accepted;
+  P.n_committed = out_n_committed;
+  P.status = status;
+  P.out_w = W;
+  P.lenience = 1.f;
+  P.guide = L > 0 ? guide : nullptr;
+  P.L = L;
+  P.ws = bind(workspace, Lw);
+  P.rows_per_seq = k + 1;
+  P.R = (long long)B * (k + 1);
+  cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+  if ((rc = prepare_workspace(workspace, Lw, B, k, V, stream)) != SPEC_OK) return rc;
+  return dtype == SPEC_BF16 ? launch<uint16_t, kGreedy>(P, stream, nullptr) : launch<float, kGreedy>(P, stream, nullptr);
 }
 
 int spec_random(uint64_t seed, int b, int j, int V, float* gumbel_u, float* gumbel_g, float* accept_u,
@@ -1287,7 +1444,7 @@ const char* spec_strerror(int status) {
   }
 }
 
-int spec_abi_version(void) { return (1 << 16) | 0; }
+int spec_abi_version(void) { return (1 << 16) | 1; }
 
 }  // extern "C"
 

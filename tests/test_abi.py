@@ -32,8 +32,8 @@ def lib():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for want in ("spec_verify", "spec_verify_ex", "spec_verify_tree", "spec_workspace_size", "spec_workspace_init",
-                 "spec_random", "spec_strerror", "spec_abi_version"):
+    for want in ("spec_verify", "spec_verify_ex", "spec_verify_tree", "spec_verify_guided", "spec_workspace_size",
+                 "spec_workspace_init", "spec_random", "spec_strerror", "spec_abi_version", "spec_verify_noalloc"):
         assert want in names, names
 
 
@@ -86,3 +86,54 @@ def test_strerror_names_every_code(lib):
     lib.spec_strerror.restype = ctypes.c_char_p
     names = {c: lib.spec_strerror(c).decode() for c in range(-8, 1)}
     assert len(set(names.values())) == 9 and lib.spec_strerror(-99).decode() == "unknown status"
+
+
+class _Aux(ctypes.Structure):
+    _fields_ = [("p_draft", ctypes.c_void_p), ("q_draft", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+                ("status", ctypes.c_void_p), ("events", ctypes.c_void_p * 4),
+                ("sequence_offset", ctypes.c_uint32), ("lenience", ctypes.c_float),
+                ("stop_ids", ctypes.c_void_p), ("n_stop", ctypes.c_int32), ("n_committed", ctypes.c_void_p),
+                ("match_mask", ctypes.c_void_p), ("n_match", ctypes.c_void_p), ("tail_runs", ctypes.c_void_p)]
+
+
+def test_abi_version_and_aux_layout(lib):
+    assert lib.spec_abi_version() == (1 << 16) | 1
+    # the 1.1 fields follow the 1.0 ones; the binding mirrors this layout
+    assert _Aux.lenience.offset == _Aux.sequence_offset.offset + 4
+    from speculative_decoding_draft_online_gb300 import _lib
+    assert [f[0] for f in _lib._Aux._fields_] == [f[0] for f in _Aux._fields_]
+    assert ctypes.sizeof(_lib._Aux) == ctypes.sizeof(_Aux)
+
+
+def test_aux_and_guided_host_errors(lib):
+    vp = ctypes.c_void_p
+    f = lib.spec_verify_ex
+    f.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float,
+                  ctypes.c_uint64, vp, vp, vp, ctypes.c_size_t, vp, ctypes.POINTER(_Aux)]
+    fake = vp(0x10000)
+    ARG, ALIGN, UNSUP = -1, -2, -5
+
+    def call(T=1.0, **kw):
+        a = _Aux()
+        for key, val in kw.items():
+            setattr(a, key, val)
+        return f(fake, fake, fake, 2, 3, 10, 0, T, 0, fake, fake, fake, 1 << 20, None, ctypes.byref(a))
+
+    assert call(lenience=0.5) == ARG
+    assert call(lenience=float("nan")) == ARG
+    assert call(lenience=float("inf")) == ARG
+    assert call(n_stop=-1) == ARG
+    assert call(n_stop=2) == ARG                                    # no stop_ids
+    assert call(n_stop=65, stop_ids=0x10000) == UNSUP
+    assert call(n_stop=1, stop_ids=0x10002) == ALIGN
+    assert call(match_mask=0x10000) == ARG                          # match outputs need greedy mode
+    assert call(n_match=0x10000) == ARG
+    assert call(tail_runs=0x10000) == ARG
+    g = lib.spec_verify_guided
+    g.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+    assert g(fake, fake, fake, 2, 3, -1, 10, 0, fake, fake, fake, None, fake, 1 << 20, None) == ARG   # L < 0
+    assert g(fake, fake, None, 2, 3, 4, 10, 0, fake, fake, fake, None, fake, 1 << 20, None) == ARG    # no guide
+    assert g(fake, fake, fake, 2, 3, 4, 10, 0, fake, fake, None, None, fake, 1 << 20, None) == ARG    # no n_committed
+    assert g(fake, fake, vp(0x10002), 2, 3, 4, 10, 0, fake, fake, fake, None, fake, 1 << 20, None) == ALIGN
+    assert g(fake, fake, fake, 2, 5000, 4, 10, 0, fake, fake, fake, None, fake, 1 << 20, None) == UNSUP

@@ -173,6 +173,26 @@ def c4(a: float, seed: int = 104, B: int = 16, k: int = 16, V: int = 64000, dtyp
                     meta=dict(gen_seed=seed, a=a, argmax=top))
 
 
+def guided_drafts(a: float, a_guide: float, L: int, seed: int = 106, B: int = 16, k: int = 16, V: int = 64000,
+                  dtype: str = BF16):
+    """Target-guided greedy verification inputs: C4's rows and drafts, plus a
+    target-side guide [B][L] aligned with the draft positions.  The guide's
+    entry i is the planted argmax of row i w.p. a_guide (positions with a row),
+    otherwise a uniform other id; past the rows it is a uniform id.  Each guide
+    ends after a uniform length in [0, L] (-1 after its end)."""
+    w = c4(a, seed=seed, B=B, k=k, V=V, dtype=dtype)
+    rng = np.random.default_rng(seed + 1)
+    top = w.meta["argmax"]
+    guide = rng.integers(0, V, size=(B, L)).astype(np.int32)
+    rows = min(L, k + 1)
+    if rows:
+        hit = rng.random(size=(B, rows)) < a_guide
+        guide[:, :rows] = np.where(hit, top[:, :rows], _other_id(rng, top[:, :rows], V))
+    length = rng.integers(0, L + 1, size=B)
+    guide[np.arange(L)[None, :] >= length[:, None]] = -1
+    return w, guide
+
+
 def tree_shape(prefix: int = 2, branches: int = 4, length: int = 8) -> np.ndarray:
     """Parents of a tree: a shared chain of ``prefix`` nodes, then ``branches``
     chains continuing it so that every root-to-leaf path has ``length`` nodes."""
