@@ -17,6 +17,16 @@ timed region.  `roofline` is for the dominant kernel (the row-statistics
 pass), timed by events the library records around it on the launch stream.
 `--impl reference` times the CPU oracle on a bounded sample of the same
 workload instead.
+
+`--workload` selects a supplementary line for the other paths (one GPU):
+c3_greedy (greedy on the C3 tensors), c3_greedy_match (the same with the
+#Match outputs and stop-token truncation), c3_lenient (the headline with
+lenience 2), c4_guided (B=16 k=16 V=64000 greedy with a 24-token target
+guide), c5_tree (B=8, 26-node trees, V=152064).  Inputs smaller than twice the
+L2 rotate over enough device copies that every step reads from HBM.  These
+steps are short next to the Python call that launches them, so they are
+captured in a CUDA graph (the library launches on the capturing stream) and
+the replays are timed.
 """
 from __future__ import annotations
 
@@ -343,6 +353,106 @@ def run_ours(args):
     return 0
 
 
+L2_BYTES = 129 * 1024 * 1024
+VARIANTS = ("c3_greedy", "c3_greedy_match", "c3_lenient", "c4_guided", "c5_tree")
+
+
+def run_variant(args):
+    """A supplementary device-timed line for another path of the library."""
+    import torch
+    import speculative_decoding_draft_online_gb300 as sv
+    import workloads as wl
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    name = args.workload
+    stops = None
+    if name.startswith("c3"):
+        w = make_inputs()
+    elif name == "c4_guided":
+        w, guide = wl.guided_drafts(0.8, 0.9, 24, seed=106)
+    else:
+        w = wl.c5()
+    elem = 2 if w.dtype == "bf16" else 4
+    rows = w.B * (w.k + 1)
+    row_bytes = rows * w.V * elem if name != "c3_lenient" else w.B * 2 * w.k * w.V * elem
+    n_copies = max(2, -(-2 * L2_BYTES // max(1, w.target.nbytes)) + 1)
+
+    def dev_logits(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    copies = [dev_logits(w.target) for _ in range(n_copies)]
+    draft = dev_logits(w.draft) if name == "c3_lenient" else None
+    tokens = torch.from_numpy(w.tokens).to(dev)
+    if name == "c3_greedy_match":
+        stops = torch.tensor([2, 3, 128001], dtype=torch.int32, device=dev)
+    if name == "c4_guided":
+        guide_d = torch.from_numpy(guide).to(dev)
+    if name == "c5_tree":
+        parents = torch.from_numpy(w.parents).to(dev)
+
+    ws = sv.workspace(w.B, w.k, w.V, sv.SPEC_BF16, dev)
+    out = torch.empty((w.B, w.k + 1), dtype=torch.int32, device=dev)
+    n = torch.empty((w.B,), dtype=torch.int32, device=dev)
+
+    def step(i):
+        t = copies[i % n_copies]
+        if name == "c3_greedy":
+            sv.verify(t, None, tokens, 0.0, 0, out_tokens=out, out_n=n, ws=ws)
+        elif name == "c3_greedy_match":
+            sv.verify_ex(t, None, tokens, 0.0, 0, out_tokens=out, out_n=n, ws=ws, match=True, committed=True,
+                         stop_ids=stops)
+        elif name == "c3_lenient":
+            sv.verify_ex(t, draft, tokens, w.temperature, w.seed, out_tokens=out, out_n=n, ws=ws, lenience=2.0)
+        elif name == "c4_guided":
+            sv.verify_guided(t, tokens, guide_d, ws=ws)
+        else:
+            sv.verify_tree(t, tokens, parents, ws=ws)
+
+    for i in range(max(args.warmup, 3)):          # also leaves the workspace prepared for these sizes
+        step(i)
+    torch.cuda.synchronize()
+    # one graph of n_copies * reps_per_graph steps, replayed until `steps` are done
+    per_graph = n_copies * max(1, 48 // n_copies)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(per_graph):
+            step(i)
+    replays = max(1, args.steps // per_graph)
+    graph.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clk:
+        start.record(stream)
+        for _ in range(replays):
+            graph.replay()
+        stop.record(stream)
+        torch.cuda.synchronize()
+    elapsed = start.elapsed_time(stop) / 1e3
+    args.steps = replays * per_graph
+    peak, peak_kind = peaks()
+    per_step = elapsed / args.steps
+    gbs = row_bytes / per_step / 1e9
+    line = {
+        "metric": f"verified rows/s ({name})", "value": rows * args.steps / elapsed, "unit": "rows/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": name, "B": w.B, "k": w.k, "V": w.V, "input_dtype": w.dtype,
+                   "timing": f"CUDA graph of {per_graph} steps, {replays} replays",
+                   "l2": f"{n_copies} device copies rotate ({w.target.nbytes / 1e6:.1f} MB each)",
+                   "row_bytes_per_step": row_bytes},
+        "roofline": {"bound": "hbm", "kernel": "whole step" if name == "c3_lenient" else "row_pass_kernel",
+                     "achieved": gbs, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": gbs / peak,
+                     "traffic": None, "algorithmic_bytes": row_bytes},
+        "gpu_launches": (2 if name == "c3_lenient" else 1) * args.steps,
+        "clocks": clk.summary(),
+        "supplementary": True,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -350,11 +460,15 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle CPU baseline leg")
+    ap.add_argument("--workload", choices=("c3",) + VARIANTS, default="c3",
+                    help="c3 is the headline; the others print a supplementary line (one GPU)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload != "c3":
+        return run_variant(args)
     return run_ours(args)
 
 
