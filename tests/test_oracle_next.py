@@ -239,3 +239,105 @@ def test_guided_bad_ids():
     t = _rows_with_argmax([1, 2, 3], 5)
     r = ox.verify_guided(t, np.array([[1, 2]], dtype=np.int32), np.array([[1, 2, 7]], dtype=np.int32), "fp32")
     assert r.status[0] == ov.STATUS_TOKEN and r.n_committed[0] == -1
+
+
+# --------------------------------------------------------- top-k / top-p ---
+
+def test_filter_top_k_by_brute_force():
+    rng = np.random.default_rng(31)
+    for _ in range(200):
+        V = int(rng.integers(2, 12))
+        x = rng.integers(-3, 4, size=V).astype(np.float64)        # many ties
+        if rng.random() < 0.3:
+            x[rng.integers(0, V)] = -np.inf
+        kk = int(rng.integers(1, V + 2))
+        f = ox.filter_row(x, 1.0, kk, 0.0)
+        fin = np.isfinite(x)
+        if kk >= fin.sum():
+            assert np.array_equal(f.keep, fin)
+            continue
+        # brute force: the k-th largest value with multiplicity, ties kept
+        kth = sorted(x[fin], reverse=True)[kk - 1]
+        assert np.array_equal(f.keep, fin & (x >= kth))
+        assert f.keep.sum() >= kk
+
+
+def test_filter_top_p_by_brute_force():
+    rng = np.random.default_rng(32)
+    for _ in range(300):
+        V = int(rng.integers(1, 10))
+        x = rng.integers(-4, 4, size=V).astype(np.float64) * 0.5
+        T = float(rng.choice([0.5, 1.0, 2.0]))
+        top_p = float(rng.choice([0.1, 0.5, 0.8, 0.95, 0.999]))
+        f = ox.filter_row(x, T, 0, top_p)
+        w = np.exp(x / T - np.max(x / T))
+        w /= w.sum()
+        # brute force over every threshold among the values: the highest one reaching top_p
+        best = None
+        for tau in sorted(set(x), reverse=True):
+            if w[x >= tau].sum() >= top_p * (1 - 1e-12):
+                best = tau
+                break
+        assert np.array_equal(f.keep, x >= best), (x, T, top_p)
+        # minimal: dropping the lowest kept value falls short of top_p
+        higher = [v for v in set(x) if v > best]
+        if higher:
+            assert w[x >= min(higher)].sum() < top_p
+
+
+def test_filter_top_k_then_top_p_and_identities():
+    x = np.array([3.0, 2.0, 2.0, 1.0, 0.0, -1.0])
+    w = np.exp(x - x.max())
+    # top-k 3 keeps the ties at 2.0 as well: {3, 2, 2}; then top-p 0.6 of that mass
+    f = ox.filter_row(x, 1.0, 3, 0.6)
+    mk = w[:3].sum()
+    assert w[0] / mk < 0.6 <= w[:3].sum() / mk
+    assert f.keep.tolist() == [True, True, True, False, False, False]
+    f = ox.filter_row(x, 1.0, 3, 0.3)
+    assert w[0] / mk >= 0.3 and f.keep.tolist() == [True] + [False] * 5
+    for kk, pp in [(0, 0.0), (0, 1.0), (6, 0.0), (10, 1.0)]:
+        assert ox.filter_row(x, 1.0, kk, pp).keep.all()
+
+
+def test_filtered_verification_is_lossless_for_the_filtered_target():
+    """On consistently filtered rows, the rule commits tokens distributed as the
+    filtered target (exact enumeration at V = 6, k = 2)."""
+    from oracle import enumerate as oenum
+    rng = np.random.default_rng(41)
+    k, V = 2, 6
+    for top_k, top_p in [(3, 0.0), (0, 0.7), (4, 0.8)]:
+        t = rng.normal(size=(k + 1, V)) * 1.5
+        d = t[:k] + rng.normal(size=(k, V))
+        logp = np.stack([ox.filtered_log_softmax(t[j], 1.0, top_k, top_p)[0] for j in range(k + 1)])
+        logq = np.stack([ox.filtered_log_softmax(d[i], 1.0, top_k, top_p)[0] for i in range(k)])
+        law = oenum.full_law(logp, logq)
+        assert sum(law.values()) == pytest.approx(1.0, abs=1e-12)
+        first = np.zeros(V)
+        for key, pr in law.items():
+            first[key[0]] += pr
+        np.testing.assert_allclose(first, np.exp(logp[0]), atol=1e-12)
+
+
+def test_verify_filtered_matches_the_plain_rule_without_filters():
+    import workloads as wl
+    w = wl.c1_tiny(seed=5)
+    a = ov.verify_stochastic(w.target, w.draft, w.tokens, w.dtype, w.temperature, 77)
+    b = ox.verify_filtered(w.target, w.draft, w.tokens, w.dtype, w.temperature, 77, 0, 0.0)
+    np.testing.assert_array_equal(a.out_tokens, b.out_tokens)
+    np.testing.assert_array_equal(a.n_accepted, b.n_accepted)
+    np.testing.assert_allclose(a.p_draft, b.p_draft, rtol=1e-12)
+
+
+def test_verify_filtered_restricts_every_committed_token():
+    """Committed tokens lie in the kept set of the target row at their position."""
+    import workloads as wl
+    w = wl.c2(seed=9)
+    r = ox.verify_filtered(w.target, w.draft, w.tokens, w.dtype, w.temperature, 3, 20, 0.9)
+    t = ov.decode_logits(w.target, w.dtype)
+    for b in range(w.B):
+        for j in range(r.n_accepted[b] + 1):
+            f = ox.filter_row(t[b, j], w.temperature, 20, 0.9)
+            tok = r.out_tokens[b, j]
+            if j < r.n_accepted[b]:
+                continue                 # an accepted draft may lie outside p's kept set only if q'(x) = 0 too
+            assert f.keep[tok], (b, j, tok)
