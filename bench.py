@@ -21,7 +21,8 @@ workload instead.
 `--workload` selects a supplementary line for the other paths (one GPU):
 c3_greedy (greedy on the C3 tensors), c3_greedy_match (the same with the
 #Match outputs and stop-token truncation), c3_lenient (the headline with
-lenience 2), c4_guided (B=16 k=16 V=64000 greedy with a 24-token target
+lenience 2), c3_top_p / c3_top_k_top_p (the headline with consistent top-p
+0.8, or top-k 50 then top-p 0.8), c4_guided (B=16 k=16 V=64000 greedy with a 24-token target
 guide), c5_tree (B=8, 26-node trees, V=152064).  Inputs smaller than twice the
 L2 rotate over enough device copies that every step reads from HBM.  These
 steps are short next to the Python call that launches them, so they are
@@ -354,7 +355,7 @@ def run_ours(args):
 
 
 L2_BYTES = 129 * 1024 * 1024
-VARIANTS = ("c3_greedy", "c3_greedy_match", "c3_lenient", "c4_guided", "c5_tree")
+VARIANTS = ("c3_greedy", "c3_greedy_match", "c3_lenient", "c3_top_p", "c3_top_k_top_p", "c4_guided", "c5_tree")
 
 
 def run_variant(args):
@@ -375,14 +376,15 @@ def run_variant(args):
         w = wl.c5()
     elem = 2 if w.dtype == "bf16" else 4
     rows = w.B * (w.k + 1)
-    row_bytes = rows * w.V * elem if name != "c3_lenient" else w.B * 2 * w.k * w.V * elem
+    stochastic = name in ("c3_lenient", "c3_top_p", "c3_top_k_top_p")
+    row_bytes = rows * w.V * elem if not stochastic else w.B * 2 * w.k * w.V * elem
     n_copies = max(2, -(-2 * L2_BYTES // max(1, w.target.nbytes)) + 1)
 
     def dev_logits(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
 
     copies = [dev_logits(w.target) for _ in range(n_copies)]
-    draft = dev_logits(w.draft) if name == "c3_lenient" else None
+    draft = dev_logits(w.draft) if stochastic else None
     tokens = torch.from_numpy(w.tokens).to(dev)
     if name == "c3_greedy_match":
         stops = torch.tensor([2, 3, 128001], dtype=torch.int32, device=dev)
@@ -404,6 +406,11 @@ def run_variant(args):
                          stop_ids=stops)
         elif name == "c3_lenient":
             sv.verify_ex(t, draft, tokens, w.temperature, w.seed, out_tokens=out, out_n=n, ws=ws, lenience=2.0)
+        elif name == "c3_top_p":
+            sv.verify_ex(t, draft, tokens, w.temperature, w.seed, out_tokens=out, out_n=n, ws=ws, top_p=0.8)
+        elif name == "c3_top_k_top_p":
+            sv.verify_ex(t, draft, tokens, w.temperature, w.seed, out_tokens=out, out_n=n, ws=ws, top_k=50,
+                         top_p=0.8)
         elif name == "c4_guided":
             sv.verify_guided(t, tokens, guide_d, ws=ws)
         else:
@@ -442,10 +449,10 @@ def run_variant(args):
                    "timing": f"CUDA graph of {per_graph} steps, {replays} replays",
                    "l2": f"{n_copies} device copies rotate ({w.target.nbytes / 1e6:.1f} MB each)",
                    "row_bytes_per_step": row_bytes},
-        "roofline": {"bound": "hbm", "kernel": "whole step" if name == "c3_lenient" else "row_pass_kernel",
+        "roofline": {"bound": "hbm", "kernel": "whole step" if stochastic else "row_pass_kernel",
                      "achieved": gbs, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": gbs / peak,
                      "traffic": None, "algorithmic_bytes": row_bytes},
-        "gpu_launches": (2 if name == "c3_lenient" else 1) * args.steps,
+        "gpu_launches": (1 + stochastic + (name in ("c3_top_p", "c3_top_k_top_p"))) * args.steps,
         "clocks": clk.summary(),
         "supplementary": True,
     }

@@ -148,6 +148,21 @@ typedef struct spec_verify_aux {
   int32_t* tail_runs;  /* greedy only, device [B] or NULL: maximal runs of matches after the */
                        /*   first mismatch (the segments a phrase harvester keeps)           */
                        /* Any of the three in stochastic mode: SPEC_ERR_ARG.                 */
+
+  /* ---- since ABI 1.2 ---- */
+
+  int32_t top_k;       /* stochastic: consistent top-k on every target and draft row ("Speculative */
+                       /*   Decoding: ...", "Logit-processor gaps"): keep the ids whose logit is   */
+                       /*   at least the k-th largest (ties kept); 0, or >= V, keeps every id      */
+  float top_p;         /* stochastic: then consistent top-p on the top-k distribution: keep the    */
+                       /*   ids at or above the largest logit whose mass at or above it reaches    */
+                       /*   top_p (ties kept); 0 or 1 keeps every id.  Both are applied after the  */
+                       /*   temperature, to target rows 0..k and draft rows 0..k-1 alike, and the  */
+                       /*   rule runs on the renormalised rows; p_draft / q_draft report the       */
+                       /*   filtered values, lse the unfiltered normalisers.  top_k < 0 or top_p   */
+                       /*   outside [0, 1]: SPEC_ERR_ARG.  Greedy mode ignores both (they never    */
+                       /*   move an argmax).  A NaN or +inf in the bonus row is SPEC_ERR_NONFINITE */
+                       /*   for the sequence when filtering, whatever n is.                        */
 } spec_verify_aux;
 
 /* spec_verify plus the auxiliary outputs in `aux` (which may be NULL). */

@@ -31,15 +31,16 @@ class SpecError(RuntimeError):
 
 
 class _Aux(ctypes.Structure):
-    """spec_verify_aux of ABI 1.1."""
+    """spec_verify_aux of ABI 1.2."""
     _fields_ = [("p_draft", ctypes.c_void_p), ("q_draft", ctypes.c_void_p), ("lse", ctypes.c_void_p),
                 ("status", ctypes.c_void_p), ("events", ctypes.c_void_p * 4),
                 ("sequence_offset", ctypes.c_uint32), ("lenience", ctypes.c_float),
                 ("stop_ids", ctypes.c_void_p), ("n_stop", ctypes.c_int32), ("n_committed", ctypes.c_void_p),
-                ("match_mask", ctypes.c_void_p), ("n_match", ctypes.c_void_p), ("tail_runs", ctypes.c_void_p)]
+                ("match_mask", ctypes.c_void_p), ("n_match", ctypes.c_void_p), ("tail_runs", ctypes.c_void_p),
+                ("top_k", ctypes.c_int32), ("top_p", ctypes.c_float)]
 
 
-ABI_MIN = (1 << 16) | 1
+ABI_MIN = (1 << 16) | 2
 
 
 def _load():
@@ -133,7 +134,8 @@ def _check(t: torch.Tensor, name: str, shape, dtype=None):
 def verify_ex(target: torch.Tensor, draft: Optional[torch.Tensor], tokens: torch.Tensor, temperature: float,
               seed: int = 0, *, out_tokens=None, out_n=None, ws=None, stream=None, aux: bool = False,
               events=None, sequence_offset: int = 0, lenience: float = 1.0,
-              stop_ids: Optional[torch.Tensor] = None, committed: bool = False, match: bool = False):
+              stop_ids: Optional[torch.Tensor] = None, committed: bool = False, match: bool = False,
+              top_k: int = 0, top_p: float = 0.0):
     """spec_verify_ex on torch tensors.
 
     target [B][k+1][V] and draft [B][k][V] (bf16 or fp32, same dtype), tokens
@@ -146,7 +148,8 @@ def verify_ex(target: torch.Tensor, draft: Optional[torch.Tensor], tokens: torch
     sequence_offset is the global index of sequence 0 when the batch is a
     shard of a larger one; lenience >= 1 loosens the stochastic accept test;
     stop_ids is an int32 CUDA tensor of stop ids (the committed tokens end at
-    the first one).
+    the first one); top_k / top_p filter every target and draft row alike
+    before the rule (stochastic mode; 0 = off).
     """
     B, k1, V = target.shape
     k = k1 - 1
@@ -169,10 +172,12 @@ def verify_ex(target: torch.Tensor, draft: Optional[torch.Tensor], tokens: torch
     extra = {}
     a = None
     if (aux or events is not None or sequence_offset or lenience != 1.0 or stop_ids is not None or committed
-            or match):
+            or match or top_k or top_p):
         a = _Aux()
         a.sequence_offset = int(sequence_offset)
         a.lenience = float(lenience)
+        a.top_k = int(top_k)
+        a.top_p = float(top_p)
         if aux:
             extra.update(p_draft=torch.zeros((B, k), dtype=torch.float32, device=dev),
                          q_draft=torch.zeros((B, k), dtype=torch.float32, device=dev),

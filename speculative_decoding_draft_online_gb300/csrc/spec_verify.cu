@@ -82,6 +82,7 @@ struct Workspace {
   Partial* row_partial;    // [R][nt]
   unsigned* row_cnt;       // [R]
   RowStat* row_stat;       // [R]
+  float2* row_filter;      // [R] filtering mode: (threshold value, ln of the kept mass relative to the max)
   unsigned* seq_cnt;       // [B]
   SeqState* seq;           // [B]
   float2* samp_partial;    // [B][ns] (best score or NaN, index bits)
@@ -122,6 +123,9 @@ struct Params {
   int32_t* tail_runs;          // greedy: [B] or null
   const int32_t* guide;        // guided greedy: [B][L] or null
   int L;
+  int filtering;               // stochastic rows go through top-k / top-p
+  int top_k;                   // 0: off
+  float top_p;                 // 0 or 1: off
   Workspace ws;
 };
 
@@ -135,15 +139,16 @@ __device__ __forceinline__ float load_elem<float>(const float* p, size_t i) { re
 
 // Virtual row r -> its address and its sequence.  Stochastic: per sequence,
 // target rows 0..k-1 then draft rows 0..k-1 (the bonus row k needs no
-// normaliser).  Greedy / tree: the sequence's target rows.
+// normaliser), then, when filtering, target row k (its filter needs one).
+// Greedy / tree: the sequence's target rows.
 template <typename T, int kMode>
 __device__ __forceinline__ const T* row_ptr(const Params& P, long long r, int& b) {
   if constexpr (kMode == kStochastic) {
-    const int twok = 2 * P.k;
-    b = (int)(r / twok);
-    const int w = (int)(r % twok);
+    b = (int)(r / P.rows_per_seq);
+    const int w = (int)(r % P.rows_per_seq);
     if (w < P.k) return (const T*)P.target + ((size_t)b * (P.k + 1) + w) * P.V;
-    return (const T*)P.draft + ((size_t)b * P.k + (w - P.k)) * P.V;
+    if (w < 2 * P.k) return (const T*)P.draft + ((size_t)b * P.k + (w - P.k)) * P.V;
+    return (const T*)P.target + ((size_t)b * (P.k + 1) + P.k) * P.V;   // filtering: the bonus row
   }
   b = (int)(r / P.rows_per_seq);
   const int j = (int)(r % P.rows_per_seq);
@@ -331,7 +336,8 @@ template <typename T>
 __device__ void accept_scan(const Params& P, int b) {
   const int lane = threadIdx.x & 31;
   const int k = P.k;
-  const long long rbase = (long long)b * 2 * k;
+  const long long rbase = (long long)b * P.rows_per_seq;
+  const long long obase = (long long)b * 2 * k;   // [B][2k] lse output
   int n = k;
   unsigned tok_bad = 0, nf_bad = 0;
   for (int base = 0; base < k; base += 32) {
@@ -348,8 +354,15 @@ __device__ void accept_scan(const Params& P, int b) {
       if (!tbad) {
         const float xt = load_elem<T>((const T*)P.target, ((size_t)b * (k + 1) + i) * P.V + x);
         const float xd = load_elem<T>((const T*)P.draft, ((size_t)b * k + i) * P.V + x);
-        const float lp = (xt - rt.m) * P.invT - rt.lnS;   // ln p_i(x_i)
-        const float lq = (xd - rd.m) * P.invT - rd.lnS;   // ln q_i(x_i)
+        float lp = (xt - rt.m) * P.invT - rt.lnS;          // ln p_i(x_i)
+        float lq = (xd - rd.m) * P.invT - rd.lnS;          // ln q_i(x_i)
+        if (P.filtering) {
+          // the filtered, renormalised rows: 0 outside the kept set
+          const float2 ft = __ldcg(P.ws.row_filter + rbase + i);
+          const float2 fd = __ldcg(P.ws.row_filter + rbase + k + i);
+          lp = xt >= ft.x ? (xt - rt.m) * P.invT - ft.y : -CUDART_INF_F;
+          lq = xd >= fd.x ? (xd - rd.m) * P.invT - fd.y : -CUDART_INF_F;
+        }
         const float u = accept_uniform(P.key, P.b0 + (uint32_t)b, i);
         // "Asymmetric lenience": keep when q <= l p, else with probability l p / q
         acc = (lq <= lp + P.ln_lenience) || (u < P.lenience * expf(lp - lq));
@@ -357,8 +370,8 @@ __device__ void accept_scan(const Params& P, int b) {
         if (P.q_draft) P.q_draft[(size_t)b * k + i] = expf(lq);
       }
       if (P.lse) {
-        P.lse[rbase + i] = rt.m * P.invT + rt.lnS;
-        P.lse[rbase + k + i] = rd.m * P.invT + rd.lnS;
+        P.lse[obase + i] = rt.m * P.invT + rt.lnS;
+        P.lse[obase + k + i] = rd.m * P.invT + rd.lnS;
       }
     }
     tok_bad |= __ballot_sync(0xffffffffu, tbad);
@@ -366,6 +379,8 @@ __device__ void accept_scan(const Params& P, int b) {
     const unsigned rej = __ballot_sync(0xffffffffu, valid && !acc);
     if (n == k && rej) n = base + __ffs(rej) - 1;
   }
+  // filtering runs over every row of the sequence, the bonus row included
+  if (P.filtering && ldcg_stat(P.ws.row_stat + rbase + 2 * k).status != SPEC_OK) nf_bad = 1;
   if (lane == 0) {
     const int st = tok_bad ? SPEC_ERR_TOKEN : nf_bad ? SPEC_ERR_NONFINITE : SPEC_OK;
     __stcg(reinterpret_cast<int2*>(P.ws.seq) + b, make_int2(n, st));
@@ -572,6 +587,14 @@ __device__ void finish_row(const Params& P, long long r, int b) {
     bad = __any_sync(0xffffffffu, bad);
     st = RowStat{m, 0.f, ix, bad ? SPEC_ERR_NONFINITE : SPEC_OK};
   }
+  if (kMode == kStochastic && P.filtering) {
+    // the filter pass takes the row from here and runs the accept scan
+    if (lane == 0) {
+      stcg_stat(P.ws.row_stat + r, st);
+      P.ws.row_cnt[r] = 0;
+    }
+    return;
+  }
   int last = 0;
   if (lane == 0) {
     stcg_stat(P.ws.row_stat + r, st);
@@ -644,6 +667,422 @@ __global__ void __launch_bounds__(kThreads) row_pass_kernel(const Params P) {
     }
     __syncthreads();
     i += t1 - t0;
+  }
+}
+
+// ------------------------------------------------------------- filtering ---
+// Consistent top-k / top-p ("Speculative Decoding: ...", "Logit-processor
+// gaps" and "Constraints must be applied consistently"; the Ouroboros page
+// samples with top-p 0.8): every target and draft row of a sequence goes
+// through the same filter before the rule.  Order: temperature, top-k, then
+// top-p on the top-k distribution.  Both are value thresholds, so ties at a
+// threshold are kept.  One CTA per row finds each threshold in two steps:
+//   1. histograms of count and mass exp((x - m) / T) by distance below the row
+//      max (m from the row pass) pick the bin where the count (top-k) or the
+//      mass (top-p) summed from the top first reaches its target.  The bins
+//      are 1/170 nat wide over the first 12 nats, where nearly all the mass
+//      lies; ids further down are only counted, in registers, and a target that
+//      lies further down is found in a second or third window of coarser bins.
+//      Only the ids near the top take shared-memory atomics, spread over many
+//      bins.
+//   2. the bin holds a contiguous range of order-preserving keys of the raw
+//      logits, found by bisection; when it spans fewer than 2048 keys (always
+//      for bf16 near the top) one pass histograms key - smallest, otherwise
+//      radix rounds over the key bits (11 a round) decide the exact value.
+// Masses are summed as 64-bit fixed point (2^-40 units) with integer atomics.
+
+constexpr int kHistBits = 11;
+constexpr int kHistBins = 1 << kHistBits;
+
+template <typename T>
+struct Keys;
+template <>
+struct Keys<uint16_t> {
+  static constexpr int kBits = 16;
+  __device__ static uint32_t of(float x) {
+    const uint32_t h = __float_as_uint(x) >> 16;
+    return (h & 0x8000u) ? (~h & 0xFFFFu) : (h | 0x8000u);
+  }
+  __device__ static float value(uint32_t k) {
+    return __uint_as_float(((k & 0x8000u) ? (k & 0x7FFFu) : (~k & 0xFFFFu)) << 16);
+  }
+};
+template <>
+struct Keys<float> {
+  static constexpr int kBits = 32;
+  __device__ static uint32_t of(float x) {
+    const uint32_t u = __float_as_uint(x);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  }
+  __device__ static float value(uint32_t k) { return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k); }
+};
+
+constexpr int kDistBins = 2048;            // step 1: bin 0 = the window's tail, bins 1..2047 (2047 = the top)
+constexpr int kWindows = 3;
+static_assert(kDistBins <= kHistBins, "the distance histogram shares the radix histogram's storage");
+
+// Step 1 looks at the scaled distance d = (m - x) / T >= 0 below the row max in
+// windows: window 0 has bins of 1/170 nat over its first 2047/170 (12) nats,
+// window 1 bins of 1/8 nat over the next 2047/8, window 2 bins of 2 nats beyond.
+__device__ __forceinline__ float win_scale(int w) { return w == 0 ? 170.f : (w == 1 ? 8.f : 0.5f); }
+__device__ __forceinline__ float win_start(int w) {
+  return w == 0 ? 0.f : (w == 1 ? 2047.f / 170.f : 2047.f / 170.f + 2047.f / 8.f);
+}
+
+// A row's windows as affine maps of the logit: window w's scaled position of x
+// is s_w(x) = fma(-x, a_w, b_w) = ((m - x) / T - start_w) * scale_w, rounded
+// once; non-increasing in x.
+struct Windows {
+  float a[kWindows], b[kWindows];
+  __device__ Windows(float m, float invT) {
+#pragma unroll
+    for (int w = 0; w < kWindows; ++w) {
+      a[w] = invT * win_scale(w);
+      b[w] = (m * invT - win_start(w)) * win_scale(w);
+    }
+  }
+  // Where x falls in window w: kDistBins if above the window (not in the tail
+  // of every earlier window), else 0 for the window's tail or its bin 1..2047.
+  // Non-decreasing in x.
+  __device__ __forceinline__ int bin(float x, int w) const {
+    for (int j = 0; j < w; ++j)
+      if (!(fmaf(-x, a[j], b[j]) >= (float)(kDistBins - 1))) return kDistBins;
+    const float s = fmaxf(fmaf(-x, a[w], b[w]), 0.f);
+    return s < (float)(kDistBins - 1) ? (kDistBins - 1) - (int)s : 0;
+  }
+};
+
+constexpr float kMassUnit = 1099511627776.0f;   // 2^40: fixed-point scale of a mass in (0, 1]
+
+struct FilterScratch {
+  uint32_t cnt[kHistBins];
+  float mass[kHistBins];
+  unsigned long long massq[kHistBins];   // fixed-point sums, turned into `mass` after a pass
+  uint32_t wc[kWarps];
+  float wm[kWarps];
+  int sel_bin;
+  uint32_t sel_cnt_above, sel_cnt_bin, total_cnt;
+  float sel_mass_above, sel_mass_bin;
+};
+
+__device__ __forceinline__ void clear_hist(FilterScratch& S, int nbins) {
+  for (int i = threadIdx.x; i < nbins; i += kThreads) {
+    S.cnt[i] = 0u;
+    S.massq[i] = 0ull;
+    S.mass[i] = 0.f;
+  }
+}
+
+__device__ __forceinline__ void fix_masses(FilterScratch& S, int nbins) {
+  for (int i = threadIdx.x; i < nbins; i += kThreads)
+    if (S.massq[i]) S.mass[i] = (float)S.massq[i] * (1.0f / kMassUnit);
+}
+
+// Step 2's histogram over the ids with keys in [klo, khi], fed by scan_segment:
+// one round over key - klo when the range is under kHistBins keys, otherwise
+// radix rounds over the key bits from the top.
+template <typename T>
+struct HistAcc {
+  FilterScratch* S;
+  uint32_t klo, khi;  // the ids taking part
+  bool one_round;
+  uint32_t prefix;    // radix rounds: the key bits decided so far
+  int shift_hi;       //   at key bits [shift_hi, kBits); kBits: none yet
+  int shift_lo;       //   this round's bits are [shift_lo, shift_hi)
+  float c, mc;        // mass = exp2(x c - mc) = exp((x - m) / T)
+  __device__ __forceinline__ void elem(float x) {
+    if (!(x > -CUDART_INF_F)) return;                  // -inf ids are never kept
+    const uint32_t key = Keys<T>::of(x);
+    if (key < klo || key > khi) return;
+    uint32_t bin;
+    if (one_round) {
+      bin = key - klo;
+    } else {
+      if (shift_hi < Keys<T>::kBits && (key >> shift_hi) != prefix) return;
+      bin = (key >> shift_lo) & ((1u << (shift_hi - shift_lo)) - 1u);
+    }
+    atomicAdd(&S->cnt[bin], 1u);
+    atomicAdd(&S->massq[bin], (unsigned long long)(ex2_approx(fmaf(x, c, -mc)) * kMassUnit));
+  }
+  template <typename TT, int U>
+  __device__ __forceinline__ void vec(const uint4 (&v)[U], const int (&)[U]) {
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int e = 0; e < Vec<T>::n; ++e) elem(Vec<T>::at(v[u], e));
+  }
+  __device__ __forceinline__ void scalar(float x, int) { elem(x); }
+};
+
+// The bin where the count (by_mass false) or the mass, summed from the top
+// bin down, first reaches `need` (clamped to the total), with the count and
+// mass of the bins above it and of the bin itself.  All threads call it.
+__device__ void select_bin(FilterScratch& S, int nbins, bool by_mass, uint32_t need_cnt, float need_mass) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int per = nbins >= kThreads ? nbins / kThreads : 1;
+  const int owners = nbins / per;
+  const int t = threadIdx.x;
+  uint32_t lc = 0;
+  float lm = 0.f;
+  if (t < owners)
+    for (int j = 0; j < per; ++j) {
+      const int bin = nbins - 1 - (t * per + j);
+      lc += S.cnt[bin];
+      lm += S.mass[bin];
+    }
+  // inclusive scan in thread order (thread 0 holds the top bins)
+  uint32_t ic = lc;
+  float im = lm;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t c2 = __shfl_up_sync(0xffffffffu, ic, o);
+    const float m2 = __shfl_up_sync(0xffffffffu, im, o);
+    if (lane >= o) { ic += c2; im += m2; }
+  }
+  if (lane == 31) { S.wc[w] = ic; S.wm[w] = im; }
+  __syncthreads();
+  uint32_t oc = 0;
+  float om = 0.f;
+  for (int q = 0; q < w; ++q) { oc += S.wc[q]; om += S.wm[q]; }
+  ic += oc;
+  im += om;
+  const uint32_t ec = ic - lc;                         // exact for counts
+  float em = __shfl_up_sync(0xffffffffu, im, 1);
+  if (lane == 0) em = om;
+  // totals as the last owner's inclusive values, so the comparisons below agree with them
+  __syncthreads();
+  if (t == owners - 1) { S.wc[0] = ic; S.wm[0] = im; }
+  __syncthreads();
+  const uint32_t tc = S.wc[0];
+  const float tm = S.wm[0];
+  bool mine;
+  if (by_mass) {
+    const float need = fminf(need_mass, tm);
+    mine = t < owners && lc > 0 && em < need && need <= im;
+    if (!(tm > 0.f)) mine = t < owners && lc > 0 && ec + lc == tc;   // no mass seen: the lowest non-empty bin
+  } else {
+    const uint32_t need = min(need_cnt, tc);
+    mine = t < owners && lc > 0 && ec < need && need <= ic;
+  }
+  if (mine) {
+    uint32_t c = ec;
+    float mm = em;
+    int pick = -1, last_nonzero = -1;
+    uint32_t pc = 0;
+    float pm = 0.f;
+    for (int j = 0; j < per; ++j) {
+      const int bin = nbins - 1 - (t * per + j);
+      const uint32_t bc = S.cnt[bin];
+      const float bm = S.mass[bin];
+      if (bc) { last_nonzero = bin; pc = c; pm = mm; }
+      if (bc && (by_mass ? (tm > 0.f && mm + bm >= fminf(need_mass, tm)) : (c + bc >= min(need_cnt, tc)))) {
+        pick = bin;
+        break;
+      }
+      c += bc;
+      mm += bm;
+    }
+    if (pick < 0) pick = last_nonzero;                // rounding left the target a hair above: the last bin
+    else { pc = c; pm = mm; }
+    S.sel_bin = pick;
+    S.sel_cnt_above = pc;
+    S.sel_mass_above = pm;
+    S.sel_cnt_bin = S.cnt[pick];
+    S.sel_mass_bin = S.mass[pick];
+  }
+  if (t == 0) S.total_cnt = tc;
+  __syncthreads();
+}
+
+// Step 1's histogram for window `win`, fed by scan_segment.
+template <typename T>
+struct DistAcc {
+  FilterScratch* S;
+  uint32_t key_min;
+  float c, mc;
+  const Windows* W;
+  int win;
+  uint32_t tail_cnt;
+  __device__ __forceinline__ void elem(float x) {
+    if (win == 0) {
+      // the common pass: one FMA and a compare for an id far below the max
+      const float s = fmaf(-x, W->a[0], W->b[0]);
+      if (!(s < (float)(kDistBins - 1))) {             // the tail, or -inf (s = +inf)
+        if (x > -CUDART_INF_F && (key_min == 0u || Keys<T>::of(x) >= key_min)) ++tail_cnt;
+        return;
+      }
+      if (key_min != 0u && Keys<T>::of(x) < key_min) return;
+      const int bin = (kDistBins - 1) - (int)fmaxf(s, 0.f);
+      atomicAdd(&S->cnt[bin], 1u);
+      atomicAdd(&S->massq[bin], (unsigned long long)(ex2_approx(fmaf(x, c, -mc)) * kMassUnit));
+      return;
+    }
+    if (!(x > -CUDART_INF_F)) return;
+    if (Keys<T>::of(x) < key_min) return;
+    const int bin = W->bin(x, win);
+    if (bin == kDistBins) return;                      // above the window: counted before
+    if (bin == 0) {                                    // the window's tail: counted only
+      ++tail_cnt;
+      return;
+    }
+    atomicAdd(&S->cnt[bin], 1u);
+    atomicAdd(&S->massq[bin], (unsigned long long)(ex2_approx(fmaf(x, c, -mc)) * kMassUnit));
+  }
+  template <typename TT, int U>
+  __device__ __forceinline__ void vec(const uint4 (&v)[U], const int (&)[U]) {
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int e = 0; e < Vec<T>::n; ++e) elem(Vec<T>::at(v[u], e));
+  }
+  __device__ __forceinline__ void scalar(float x, int) { elem(x); }
+};
+
+// The largest key whose count (by_mass false) or mass of ids at or above it,
+// among the ids with key >= key_min, reaches the target.  Returns false when
+// the count target is at least the number of those ids (no threshold).
+template <typename T>
+__device__ bool find_threshold(const T* row, const Params& P, const RowStat& rs, FilterScratch& S, bool by_mass,
+                               uint32_t need_cnt, float need_mass, uint32_t key_min, uint32_t& key, float& mass_ge) {
+  // step 1: the distance bin, window by window until the target falls in a bin
+  uint32_t cnt_above = 0;
+  float mass_above = 0.f, bin_mass = 0.f;
+  int win = 0, dbin = 0;
+  const Windows W(rs.m, P.invT);
+  for (; win < kWindows; ++win) {
+    clear_hist(S, kDistBins);
+    __syncthreads();
+    DistAcc<T> da{&S, key_min, P.c, rs.m * P.c, &W, win, 0u};
+    scan_segment<T>(row, 0, P.V, da);
+    const uint32_t tc = __reduce_add_sync(0xffffffffu, da.tail_cnt);
+    if ((threadIdx.x & 31) == 0 && tc) atomicAdd(&S.cnt[0], tc);
+    __syncthreads();
+    fix_masses(S, kDistBins);
+    __syncthreads();
+    // the tail's mass is not summed: a mass target beyond the bins clamps to
+    // their total and lands on the tail, and the next window takes it up
+    select_bin(S, kDistBins, by_mass, need_cnt - cnt_above, need_mass - mass_above);
+    if (win == 0 && !by_mass && S.total_cnt <= need_cnt) return false;
+    dbin = S.sel_bin;
+    cnt_above += S.sel_cnt_above;
+    mass_above += S.sel_mass_above;
+    bin_mass = S.sel_mass_bin;
+    __syncthreads();
+    if (dbin > 0) break;
+  }
+  if (win == kWindows) win = kWindows - 1;
+  // the bin's key range: its position is non-decreasing in the key over the
+  // finite values up to the max
+  if (threadIdx.x == 0) {
+    auto ord = [&](uint32_t k) { return W.bin(Keys<T>::value(k), win); };
+    uint32_t a = Keys<T>::of(-CUDART_INF_F) + 1, z = Keys<T>::of(rs.m);
+    if (a < key_min) a = key_min;
+    uint32_t l = a, h = z;                            // smallest key at or above the bin
+    while (l < h) {
+      const uint32_t mid = l + (h - l) / 2;
+      if (ord(mid) >= dbin) h = mid; else l = mid + 1;
+    }
+    uint32_t l2 = l, h2 = z;                          // largest key at or below it
+    while (l2 < h2) {
+      const uint32_t mid = l2 + (h2 - l2 + 1) / 2;
+      if (ord(mid) <= dbin) l2 = mid; else h2 = mid - 1;
+    }
+    S.wc[0] = l;
+    S.wc[1] = l2;
+  }
+  __syncthreads();
+  const uint32_t lo = S.wc[0], hi = S.wc[1];
+  __syncthreads();
+  if (dbin > 0 && lo == hi) {
+    // one key in the bin (the usual case near the top): step 1 has it all
+    key = lo;
+    mass_ge = mass_above + bin_mass;
+    return true;
+  }
+  // step 2: the exact key among the ids of that bin
+  HistAcc<T> acc{&S, lo, hi, hi - lo < (uint32_t)kHistBins, 0u, Keys<T>::kBits, 0, P.c, rs.m * P.c};
+  constexpr int kBits = Keys<T>::kBits;
+  uint32_t prefix = 0;
+  int decided = acc.one_round ? kBits : 0;
+  float mb = 0.f;
+  do {
+    const int w = acc.one_round ? kHistBits : min(kHistBits, kBits - decided);
+    const int nbins = 1 << w;
+    clear_hist(S, nbins);
+    __syncthreads();
+    acc.prefix = prefix;
+    acc.shift_hi = kBits - decided;
+    acc.shift_lo = kBits - decided - w;
+    scan_segment<T>(row, 0, P.V, acc);
+    __syncthreads();
+    fix_masses(S, nbins);
+    __syncthreads();
+    select_bin(S, nbins, by_mass, need_cnt - cnt_above, need_mass - mass_above);
+    if (acc.one_round) {
+      prefix = lo + (uint32_t)S.sel_bin;
+    } else {
+      prefix = (prefix << w) | (uint32_t)S.sel_bin;
+      decided += w;
+    }
+    cnt_above += S.sel_cnt_above;
+    mass_above += S.sel_mass_above;
+    mb = S.sel_mass_bin;
+    __syncthreads();
+  } while (decided < kBits);
+  key = prefix;
+  mass_ge = mass_above + mb;
+  return true;
+}
+
+// One CTA per row: its threshold and kept mass; the CTA that filters a
+// sequence's last row runs the sequence's accept scan on the filtered rows.
+template <typename T>
+__global__ void __launch_bounds__(kThreads) filter_kernel(const Params P) {
+  __shared__ FilterScratch S;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // the row pass's statistics must be visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const long long r = blockIdx.x;
+  int b;
+  const T* row = row_ptr<T, kStochastic>(P, r, b);
+  const RowStat rs = ldcg_stat(P.ws.row_stat + r);
+  float tau = -CUDART_INF_F, lnM = rs.lnS;
+  if (rs.status == SPEC_OK) {
+    float mass = __expf(rs.lnS);                       // the row's mass relative to its max
+    uint32_t key = 0, key_min = 0;
+    bool thr = false;
+    if (P.top_k > 0) {
+      float mk;
+      if (find_threshold<T>(row, P, rs, S, false, (uint32_t)P.top_k, 0.f, 0u, key, mk)) {
+        thr = true;
+        mass = mk;
+        key_min = key;
+      }
+    }
+    if (P.top_p > 0.f && P.top_p < 1.f) {
+      float mp;
+      find_threshold<T>(row, P, rs, S, true, 0u, P.top_p * mass, key_min, key, mp);
+      thr = true;
+      mass = mp;
+    }
+    if (thr) {
+      tau = Keys<T>::value(key);
+      lnM = logf(mass);
+    }
+  }
+  if (threadIdx.x < 32) {
+    int last = 0;
+    if (threadIdx.x == 0) {
+      __stcg(P.ws.row_filter + r, make_float2(tau, lnM));
+      __threadfence();
+      last = atomicAdd(P.ws.seq_cnt + b, 1u) + 1 == (unsigned)P.rows_per_seq;
+      if (last) P.ws.seq_cnt[b] = 0;
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (last) {
+      __threadfence();
+      accept_scan<T>(P, b);
+    }
   }
 }
 
@@ -720,14 +1159,18 @@ __device__ __forceinline__ float group_max(const Raw4<T>& r, int cnt) {
 // What a sampling CTA knows about its sequence's row.
 struct SampleRow {
   bool resid;
-  float mt, lnSt;       // target row statistics (residual)
+  float mt, lnSt;       // target row statistics (residual; lnSt of the kept mass when filtering)
   float cdelta;         // delta_v = fma(x_d - x_t, 1/T, cdelta)
+  float tau_t, tau_d;   // filtering: the kept sets are x_t >= tau_t (sampled row) and x_d >= tau_d;
+                        // -inf without filtering
 };
 
 // Exact score of id v (or -inf if it is no candidate) from its logits and noise uniform.
 __device__ __forceinline__ float exact_score(float invT, const SampleRow& R, float xt, float xd, float u) {
+  if (!(xt >= R.tau_t)) return -CUDART_INF_F;
   if (R.resid) {
-    const float delta = fmaf(xd - xt, invT, R.cdelta);
+    // q = 0 outside the draft's kept set: delta = -inf, ln(1 - e^delta) = 0
+    const float delta = xd >= R.tau_d ? fmaf(xd - xt, invT, R.cdelta) : -CUDART_INF_F;
     if (!(delta < 0.f)) return -CUDART_INF_F;
     const float lp = (xt - R.mt) * invT - R.lnSt;
     return lp + logf(-expm1f(delta)) + gumbel_of(u);
@@ -755,10 +1198,10 @@ struct Draw {
 __device__ __forceinline__ bool bound_of(const Draw& D, float x, float xdv, float& h) {
   if (D.R.resid) {
     h = (x - D.R.mt) * D.invT - D.R.lnSt;
-    return fmaf(xdv - x, D.invT, D.R.cdelta) < 0.f;
+    return x >= D.R.tau_t && (xdv < D.R.tau_d || fmaf(xdv - x, D.invT, D.R.cdelta) < 0.f);
   }
   h = x * D.invT;
-  return x > -CUDART_INF_F;
+  return x > -CUDART_INF_F && x >= D.R.tau_t;
 }
 
 // The lowest target logit that can still reach score fl: bound + G_max >= fl.
@@ -904,6 +1347,7 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const Params P) {
   D.j = n < k ? n : k;
   D.R.resid = n < k;
   D.R.mt = D.R.lnSt = D.R.cdelta = 0.f;
+  D.R.tau_t = D.R.tau_d = -CUDART_INF_F;
   const T* trow = (const T*)P.target + ((size_t)b * (k + 1) + (active ? D.j : 0)) * P.V;
   const T* drow = D.R.resid ? (const T*)P.draft + ((size_t)b * k + (active ? n : 0)) * P.V : nullptr;
   // bulk copies need 16-byte aligned rows and tiles of whole 16-byte units
@@ -930,13 +1374,24 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const Params P) {
   // the CTA's own tiles do not depend on the floor tile: start them now
   if (bulk && threadIdx.x == 0)
     for (int i = D.R.resid ? 1 : 0; i < min(m, kStages); ++i) issue(i);
+  if (active && !D.R.resid && P.filtering)
+    D.R.tau_t = __ldcg(P.ws.row_filter + (long long)b * P.rows_per_seq + 2 * k).x;   // the bonus row's filter
   if (active && D.R.resid) {
-    const long long rt_i = (long long)b * 2 * k + n;
+    const long long rt_i = (long long)b * P.rows_per_seq + n;
     const RowStat rt = ldcg_stat(P.ws.row_stat + rt_i);
     const RowStat rd = ldcg_stat(P.ws.row_stat + rt_i + k);
+    float lnSt = rt.lnS, lnSd = rd.lnS;
+    if (P.filtering) {
+      const float2 ft2 = __ldcg(P.ws.row_filter + rt_i);
+      const float2 fd2 = __ldcg(P.ws.row_filter + rt_i + k);
+      D.R.tau_t = ft2.x;
+      D.R.tau_d = fd2.x;
+      lnSt = ft2.y;
+      lnSd = fd2.y;
+    }
     D.R.mt = rt.m;
-    D.R.lnSt = rt.lnS;
-    D.R.cdelta = -(rd.m - rt.m) * P.invT - (rd.lnS - rt.lnS);
+    D.R.lnSt = lnSt;
+    D.R.cdelta = -(rd.m - rt.m) * P.invT - (lnSd - lnSt);
     const Partial* piece = P.ws.row_partial + rt_i * P.nt;
     float bm = -CUDART_INF_F;
     int bi = INT_MAX;
@@ -1068,7 +1523,9 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const Params P) {
       const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
       for (int e = 0; e < 4 && 4 * g + e < P.V; ++e) {
         const int v = 4 * g + e;
-        const float sc = load_elem<T>(row, v) * P.invT + gumbel_of(uniform_of(ws[e]));
+        const float x = load_elem<T>(row, v);
+        if (!(x >= D.R.tau_t)) continue;             // filtering: only the kept ids of p_n
+        const float sc = x * P.invT + gumbel_of(uniform_of(ws[e]));
         if (beats(sc, v, best, bidx)) { best = sc; bidx = v; }
       }
     }
@@ -1105,7 +1562,7 @@ __global__ void random_kernel(uint2 key, int b, int j, int V, float* gu, float* 
 // --------------------------------------------------------------- host side ---
 
 struct Layout {
-  size_t row_partial, row_cnt, row_stat, seq_cnt, seq, samp_partial, samp_cnt, samp_floor, total;
+  size_t row_partial, row_cnt, row_stat, row_filter, seq_cnt, seq, samp_partial, samp_cnt, samp_floor, total;
   int nt;
   long long rmax;
 };
@@ -1115,12 +1572,13 @@ static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 static bool make_layout(int B, int k, int V, Layout& L) {
   if (B <= 0 || k <= 0 || V <= 0) return false;
   L.nt = (V + kPartTile - 1) / kPartTile;
-  L.rmax = (long long)B * (long long)(2 * k > k + 1 ? 2 * k : k + 1);
+  L.rmax = (long long)B * (long long)(2 * k + 1);   // the most rows any mode takes statistics of
   size_t off = 0;
   auto take = [&](size_t bytes) { const size_t o = off; off = align_up(off + bytes, 256); return o; };
   L.row_partial = take((size_t)L.rmax * L.nt * sizeof(Partial));
   L.row_cnt = take((size_t)L.rmax * sizeof(unsigned));
   L.row_stat = take((size_t)L.rmax * sizeof(RowStat));
+  L.row_filter = take((size_t)L.rmax * sizeof(float2));
   L.seq_cnt = take((size_t)B * sizeof(unsigned));
   L.seq = take((size_t)B * sizeof(SeqState));
   L.samp_partial = take((size_t)B * L.nt * sizeof(float2));
@@ -1136,6 +1594,7 @@ static Workspace bind(void* base, const Layout& L) {
   w.row_partial = reinterpret_cast<Partial*>(p + L.row_partial);
   w.row_cnt = reinterpret_cast<unsigned*>(p + L.row_cnt);
   w.row_stat = reinterpret_cast<RowStat*>(p + L.row_stat);
+  w.row_filter = reinterpret_cast<float2*>(p + L.row_filter);
   w.seq_cnt = reinterpret_cast<unsigned*>(p + L.seq_cnt);
   w.seq = reinterpret_cast<SeqState*>(p + L.seq);
   w.samp_partial = reinterpret_cast<float2*>(p + L.samp_partial);
@@ -1212,13 +1671,22 @@ static int launch(Params& P, cudaStream_t stream, const spec_verify_aux* aux) {
     if (slots <= 0) return SPEC_ERR_CUDA;
     P.ns = slots / P.B;
     P.ns = P.ns < 1 ? 1 : (P.ns > P.nt ? P.nt : P.ns);
-    if (rec(2) != cudaSuccess) return SPEC_ERR_CUDA;
-    // launched as a programmatic dependent of the row pass: its CTAs may start
-    // while the row pass drains and wait for its results in griddepcontrol.wait
-    cudaLaunchConfig_t cfg = {};
+    // launched as programmatic dependents of the kernel before them: their CTAs
+    // may start while it drains and wait for its results in griddepcontrol.wait
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    if (P.filtering) {
+      cudaLaunchConfig_t fcfg = {};
+      fcfg.gridDim = dim3((unsigned)P.R);
+      fcfg.blockDim = dim3(kThreads);
+      fcfg.stream = stream;
+      fcfg.attrs = attr;
+      fcfg.numAttrs = 1;
+      if (cudaLaunchKernelEx(&fcfg, filter_kernel<T>, P) != cudaSuccess) return SPEC_ERR_CUDA;
+    }
+    if (rec(2) != cudaSuccess) return SPEC_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(P.B * P.ns));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
@@ -1278,7 +1746,12 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, const in
   if (!aligned(draft_tokens, 4) || !aligned(out_tokens, 4) || !aligned(out_n_accepted, 4)) return SPEC_ERR_ALIGN;
 
   float lenience = 1.f;
+  int top_k = 0;
+  float top_p = 0.f;
   if (aux) {
+    if (aux->top_k < 0 || !(aux->top_p >= 0.f && aux->top_p <= 1.f)) return SPEC_ERR_ARG;
+    top_k = aux->top_k < V ? aux->top_k : 0;          // k >= V keeps every id
+    top_p = aux->top_p < 1.f ? aux->top_p : 0.f;      // 1 keeps every id
     if (aux->lenience != 0.f) {
       if (!(aux->lenience >= 1.f) || !std::isfinite(aux->lenience)) return SPEC_ERR_ARG;
       lenience = aux->lenience;
@@ -1327,8 +1800,13 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, const in
     P.R = (long long)B * (k + 1);
     return dtype == SPEC_BF16 ? launch<uint16_t, kGreedy>(P, stream, aux) : launch<float, kGreedy>(P, stream, aux);
   }
-  P.rows_per_seq = 2 * k;
-  P.R = (long long)B * 2 * k;
+  // filtering (stochastic only: it leaves every argmax where it is) also needs
+  // the bonus row's statistics
+  P.filtering = (top_k > 0 || top_p > 0.f) ? 1 : 0;
+  P.top_k = top_k;
+  P.top_p = top_p;
+  P.rows_per_seq = 2 * k + P.filtering;
+  P.R = (long long)B * P.rows_per_seq;
   P.invT = 1.0f / temperature;
   P.T = temperature;
   P.c = (float)(1.4426950408889634 / (double)temperature);
@@ -1444,7 +1922,7 @@ const char* spec_strerror(int status) {
   }
 }
 
-int spec_abi_version(void) { return (1 << 16) | 1; }
+int spec_abi_version(void) { return (1 << 16) | 2; }
 
 }  // extern "C"
 

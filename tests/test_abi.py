@@ -93,11 +93,12 @@ class _Aux(ctypes.Structure):
                 ("status", ctypes.c_void_p), ("events", ctypes.c_void_p * 4),
                 ("sequence_offset", ctypes.c_uint32), ("lenience", ctypes.c_float),
                 ("stop_ids", ctypes.c_void_p), ("n_stop", ctypes.c_int32), ("n_committed", ctypes.c_void_p),
-                ("match_mask", ctypes.c_void_p), ("n_match", ctypes.c_void_p), ("tail_runs", ctypes.c_void_p)]
+                ("match_mask", ctypes.c_void_p), ("n_match", ctypes.c_void_p), ("tail_runs", ctypes.c_void_p),
+                ("top_k", ctypes.c_int32), ("top_p", ctypes.c_float)]
 
 
 def test_abi_version_and_aux_layout(lib):
-    assert lib.spec_abi_version() == (1 << 16) | 1
+    assert lib.spec_abi_version() == (1 << 16) | 2
     # the 1.1 fields follow the 1.0 ones; the binding mirrors this layout
     assert _Aux.lenience.offset == _Aux.sequence_offset.offset + 4
     from speculative_decoding_draft_online_gb300 import _lib
@@ -129,6 +130,10 @@ def test_aux_and_guided_host_errors(lib):
     assert call(match_mask=0x10000) == ARG                          # match outputs need greedy mode
     assert call(n_match=0x10000) == ARG
     assert call(tail_runs=0x10000) == ARG
+    assert call(top_k=-1) == ARG
+    assert call(top_p=-0.1) == ARG
+    assert call(top_p=1.5) == ARG
+    assert call(top_p=float("nan")) == ARG
     g = lib.spec_verify_guided
     g.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                   vp, vp, vp, vp, vp, ctypes.c_size_t, vp]

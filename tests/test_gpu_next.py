@@ -187,3 +187,68 @@ def test_margin_rows_under_one_in_ten_thousand():
     if TALLY.rows < 10_000:
         pytest.skip(f"only {TALLY.rows} positions compared in this run (a subset was selected)")
     assert TALLY.margin_rows < 1e-4 * TALLY.rows, TALLY
+
+
+# ---------------------------------------------------------- top-k / top-p ---
+
+def _filtered(sv, w, seed, top_k, top_p, target=None, draft=None):
+    tgt = w.target if target is None else target
+    drf = w.draft if draft is None else draft
+    t, d, x = to_device(tgt, w.dtype), to_device(drf, w.dtype), tokens_to_device(w.tokens)
+    out, n, aux = sv.verify_ex(t, d, x, w.temperature, seed, aux=True, top_k=top_k, top_p=top_p)
+    torch.cuda.synchronize()
+    ref = ox.verify_filtered(tgt, drf, w.tokens, w.dtype, w.temperature, seed, top_k, top_p)
+    TALLY.add(compare_stochastic(ref, out.cpu().numpy(), n.cpu().numpy(), aux["status"].cpu().numpy(), w.k))
+    # filtered p_i(x_i), q_i(x_i) where no row of the sequence sits on a top-p boundary
+    ok = (ref.status == 0) & np.all(ref.filter_margin >= 1e-5, axis=1)
+    if ok.any():
+        p = aux["p_draft"].cpu().numpy().astype(np.float64)
+        q = aux["q_draft"].cpu().numpy().astype(np.float64)
+        assert np.max(np.abs(p[ok] - ref.p_draft[ok])) < 1e-5
+        assert np.max(np.abs(q[ok] - ref.q_draft[ok])) < 1e-5
+    return ref, out.cpu().numpy(), n.cpu().numpy()
+
+
+@pytest.mark.parametrize("top_k,top_p", [(50, 0.0), (0, 0.8), (200, 0.9), (1, 0.0), (0, 0.02), (7, 0.5)])
+def test_filtered_c2(sv, top_k, top_p):
+    for s in range(8):
+        w = wl.c2(seed=500 + s)
+        _filtered(sv, w, 2000 + s, top_k, top_p)
+
+
+def test_filtered_c3_top_p(sv):
+    w = wl.c3()
+    ref, out, n = _filtered(sv, w, w.seed, 0, 0.8)
+    # the filter leaves fewer ids, so drafts outside the target's kept set get rejected
+    assert (ref.status == 0).all()
+
+
+def test_filtered_fp32_c1(sv):
+    for s in range(10):
+        w = wl.c1_tiny(seed=600 + s)
+        _filtered(sv, w, 77 + s, 40, 0.95)
+        _filtered(sv, w, 77 + s, 0, 0.6)
+
+
+def test_filtered_ties_and_masked_vocabulary(sv):
+    rng = np.random.default_rng(12)
+    B, k, V = 6, 4, 3000
+    t = np.round(rng.normal(size=(B, k + 1, V)) * 2) / 2         # heavy ties
+    t[:, :, rng.random(V) < 0.3] = -np.inf                         # masked ids
+    d = t[:, :k] + np.round(rng.normal(size=(B, k, V))) / 2
+    d[np.isneginf(t[:, :k])] = -np.inf
+    from workloads import store, BF16, Workload
+    toks = np.argmax(d, axis=-1).astype(np.int32)
+    w = Workload("ties", "stochastic", B, k, V, BF16, 1.0, store(t.astype(np.float32), BF16),
+                 store(d.astype(np.float32), BF16), toks)
+    for top_k, top_p in [(1, 0.0), (5, 0.0), (0, 0.3), (10, 0.7)]:
+        _filtered(sv, w, 31, top_k, top_p)
+
+
+def test_filtering_is_ignored_in_greedy_mode(sv):
+    w = wl.c4(0.8, seed=3, B=4, k=6, V=2000)
+    t, x = to_device(w.target, w.dtype), tokens_to_device(w.tokens)
+    o1, n1 = sv.verify(t, None, x, 0.0, 0)
+    o2, n2, _ = sv.verify_ex(t, None, x, 0.0, 0, top_k=3, top_p=0.5, committed=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(n1, n2)
