@@ -614,8 +614,36 @@ __device__ void finish_row(const Params& P, long long r, int b) {
 
 // --------------------------------------------------------------- row pass ---
 
+// A CTA has finished its piece [t0, t1) of row r with partial `part`: store it
+// (the piece's other tiles get a neutral partial) and, if that completes the
+// row, merge the row in warp 0.
 template <typename T, int kMode>
-__global__ void __launch_bounds__(kThreads) row_pass_kernel(const Params P) {
+__device__ __forceinline__ void end_piece(const Params& P, long long r, int b, int t0, int t1, const float4& part) {
+  if (threadIdx.x >= 32) return;
+  int last = 0;
+  if (threadIdx.x == 0) {
+    float4* dst = reinterpret_cast<float4*>(P.ws.row_partial + r * P.nt);
+    __stcg(dst + t0, part);
+    // the piece's other tiles: nothing to add to the sums or the argmax
+    const float4 neutral = make_float4(-CUDART_INF_F, 0.f, __int_as_float(INT_MAX), 0.f);
+    for (int u = t0 + 1; u < t1; ++u) __stcg(dst + u, neutral);
+    __threadfence();
+    const unsigned add = (unsigned)(t1 - t0);
+    last = atomicAdd(P.ws.row_cnt + r, add) + add == (unsigned)P.nt;
+  }
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (last) finish_row<T, kMode>(P, r, b);
+}
+
+// Resident CTAs per SM the row pass is compiled for. Six 256-thread CTAs of
+// 16-bit rows (40 registers a thread, no spills) keep more loads in flight than
+// the four the default register budget allows; fp32 rows keep four, since their
+// argmax modes would spill at six.
+template <typename T>
+constexpr int kRowPassMinCtas = sizeof(T) == 2 ? 6 : 4;
+
+template <typename T, int kMode>
+__global__ void __launch_bounds__(kThreads, kRowPassMinCtas<T>) row_pass_kernel(const Params P) {
   __shared__ BlockScratch sh;
   // the sampling launch may be scheduled as this grid's CTAs retire; it waits
   // for this grid's results before reading them
@@ -650,21 +678,7 @@ __global__ void __launch_bounds__(kThreads) row_pass_kernel(const Params P) {
       block_argmax_flag(v, ix, bad, sh);
       part = make_float4(bad ? CUDART_NAN_F : v, 0.f, __int_as_float(ix), 0.f);
     }
-    if (threadIdx.x < 32) {
-      int last = 0;
-      if (threadIdx.x == 0) {
-        float4* dst = reinterpret_cast<float4*>(P.ws.row_partial + r * P.nt);
-        __stcg(dst + t0, part);
-        // the piece's other tiles: nothing to add to the sums or the argmax
-        const float4 neutral = make_float4(-CUDART_INF_F, 0.f, __int_as_float(INT_MAX), 0.f);
-        for (int u = t0 + 1; u < t1; ++u) __stcg(dst + u, neutral);
-        __threadfence();
-        const unsigned add = (unsigned)(t1 - t0);
-        last = atomicAdd(P.ws.row_cnt + r, add) + add == (unsigned)P.nt;
-      }
-      last = __shfl_sync(0xffffffffu, last, 0);
-      if (last) finish_row<T, kMode>(P, r, b);
-    }
+    end_piece<T, kMode>(P, r, b, t0, t1, part);
     __syncthreads();
     i += t1 - t0;
   }
@@ -1285,22 +1299,6 @@ __device__ __forceinline__ void score_tile(const Draw& D, int v0, int v1, const 
   __syncwarp();   // the queue is refilled by the next tile
 }
 
-constexpr long long kWaitLimitNs = 1000000000LL;   // 1 s: a bulk copy that has not landed by then never will
-
-__device__ __forceinline__ long long global_ns() {
-  long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-// Wait for phase `parity` of `bar`; false if it did not complete within the limit.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = global_ns();
-  while (!mbar_try_wait(bar, parity))
-    if (global_ns() - t0 > kWaitLimitNs) return false;
-  return true;
-}
 
 // One sequence's draw runs on ns CTAs over the row pass's 4096-id tiles.
 //
@@ -1627,9 +1625,9 @@ static int prepare_workspace(void* ws, const Layout& L, int B, int k, int V, cud
   return SPEC_OK;
 }
 
-// Resident CTAs of a kernel with `smem` bytes of dynamic shared memory on the
-// current device, cached per (device, kernel).
-static int resident_ctas(const void* fn, size_t smem = 0) {
+// Resident CTAs of a kernel with `threads` threads and `smem` bytes of dynamic
+// shared memory on the current device, cached per (device, kernel).
+static int resident_ctas(const void* fn, size_t smem = 0, int threads = kThreads) {
   static std::mutex mu;
   static struct Entry { int dev; const void* fn; int ctas; } cache[64];
   static int used = 0;
@@ -1643,7 +1641,7 @@ static int resident_ctas(const void* fn, size_t smem = 0) {
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem) != cudaSuccess) return 0;
   const int ctas = sms * (per_sm > 0 ? per_sm : 1);
   if (used < 64) cache[used++] = Entry{dev, fn, ctas};
   return ctas;
@@ -1655,10 +1653,9 @@ static int launch(Params& P, cudaStream_t stream, const spec_verify_aux* aux) {
     return (aux && aux->events[i]) ? cudaEventRecord(static_cast<cudaEvent_t>(aux->events[i]), stream)
                                    : cudaSuccess;
   };
-  const void* rp = reinterpret_cast<const void*>(&row_pass_kernel<T, kMode>);
-  const int ctas = resident_ctas(rp);
-  if (ctas <= 0) return SPEC_ERR_CUDA;
   const long long items = P.R * P.nt;
+  const int ctas = resident_ctas(reinterpret_cast<const void*>(&row_pass_kernel<T, kMode>));
+  if (ctas <= 0) return SPEC_ERR_CUDA;
   const int grid = (int)(items < ctas ? items : ctas);
   if (rec(0) != cudaSuccess) return SPEC_ERR_CUDA;
   row_pass_kernel<T, kMode><<<grid, kThreads, 0, stream>>>(P);
