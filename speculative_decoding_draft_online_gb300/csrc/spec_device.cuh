@@ -174,36 +174,47 @@ __device__ __forceinline__ void block_argmax(float& v, int& i, BlockScratch& sh)
   i = bi;
 }
 
+// Barrier over the reducing threads: the whole CTA, or (kNamed) named barrier
+// 1 over the first kThreads threads, for kernels whose extra warps do not
+// take part.
+template <bool kNamed>
+__device__ __forceinline__ void reducers_sync() {
+  if constexpr (kNamed) asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
+  else __syncthreads();
+}
+
 // (max, sum, bad-flag) over the CTA in one pass: two barriers.
+template <bool kNamed = false>
 __device__ __forceinline__ void block_lse_flag(float& m, float& s, int& bad, float c, BlockScratch& sh) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const float M = warp_max(m);
   s = warp_sum(rescale(s, m, M, c));
   const int wb = __any_sync(0xffffffffu, bad);
   if (lane == 0) { sh.f[w] = M; sh.g[w] = s; sh.i[w] = wb; }
-  __syncthreads();
+  reducers_sync<kNamed>();
   const float bm = (lane < kWarps) ? sh.f[lane] : -CUDART_INF_F;
   float bs = (lane < kWarps) ? sh.g[lane] : 0.f;
   bad = __any_sync(0xffffffffu, lane < kWarps && sh.i[lane]);
   const float BM = warp_max(bm);
   bs = warp_sum(rescale(bs, bm, BM, c));
-  __syncthreads();
+  reducers_sync<kNamed>();
   m = BM;
   s = bs;
 }
 
 // (value, lowest index, bad-flag) over the CTA in one pass: two barriers.
+template <bool kNamed = false>
 __device__ __forceinline__ void block_argmax_flag(float& v, int& i, int& bad, BlockScratch& sh) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   warp_argmax(v, i);
   const int wb = __any_sync(0xffffffffu, bad);
   if (lane == 0) { sh.f[w] = v; sh.i[w] = i; sh.g[w] = __int_as_float(wb); }
-  __syncthreads();
+  reducers_sync<kNamed>();
   float bv = (lane < kWarps) ? sh.f[lane] : -CUDART_INF_F;
   int bi = (lane < kWarps) ? sh.i[lane] : 0x7fffffff;
   bad = __any_sync(0xffffffffu, lane < kWarps && __float_as_int(sh.g[lane]));
   warp_argmax(bv, bi);
-  __syncthreads();
+  reducers_sync<kNamed>();
   v = bv;
   i = bi;
 }

@@ -25,17 +25,21 @@
 //               partials in one warp; the one that completes a sequence runs
 //               its per-sequence step in that warp: the accept scan (one
 //               position per lane, first rejection by ballot), the greedy
-//               match, or the tree walk.
+//               match, or the tree walk.  Greedy and tree batches of aligned
+//               rows larger than L2 stream through a ring of bulk copies into
+//               shared memory instead, fed by a producer warp.
 //   sampling    stochastic mode, a second launch that starts while the row
-//               pass drains (programmatic dependent launch): one CTA per 8192
-//               ids of the row each sequence needs (the rejected position's
-//               target and draft rows, or the bonus row), scoring
+//               pass drains (programmatic dependent launch): for each sequence,
+//               as many CTAs as fill the GPU once share the 4096-id tiles of the
+//               rows it needs (the rejected position's target and draft rows,
+//               or the bonus row), staged by bulk copies, scoring
 //               ln max(0, p - q) + Gumbel, or z + Gumbel, with Philox noise,
 //               pruned exactly against the best score reached so far; the
 //               last CTA of a sequence merges and writes the committed tokens.
 //
-// No kernel waits on a flag another CTA sets; completion is detected with
-// atomic counters by whichever CTA finishes last.
+// No kernel waits on a flag another CTA sets (the bulk-copy waits are on the
+// CTA's own barriers, bounded); completion is detected with atomic counters by
+// whichever CTA finishes last.
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -339,17 +343,18 @@ __device__ void accept_scan(const Params& P, int b) {
   const long long rbase = (long long)b * P.rows_per_seq;
   const long long obase = (long long)b * 2 * k;   // [B][2k] lse output
   int n = k;
-  unsigned tok_bad = 0, nf_bad = 0;
+  unsigned tok_bad = 0, nf_bad = 0, to_bad = 0;
   for (int base = 0; base < k; base += 32) {
     const int i = base + lane;
     const bool valid = i < k;
     bool acc = true;
-    bool tbad = false, fbad = false;
+    bool tbad = false, fbad = false, tmo = false;
     if (valid) {
       const int x = P.tokens[(size_t)b * k + i];
       const RowStat rt = ldcg_stat(P.ws.row_stat + rbase + i);
       const RowStat rd = ldcg_stat(P.ws.row_stat + rbase + k + i);
       fbad = rt.status != SPEC_OK || rd.status != SPEC_OK;
+      tmo = rt.status == SPEC_ERR_TIMEOUT || rd.status == SPEC_ERR_TIMEOUT;
       tbad = x < 0 || x >= P.V;
       if (!tbad) {
         const float xt = load_elem<T>((const T*)P.target, ((size_t)b * (k + 1) + i) * P.V + x);
@@ -376,13 +381,18 @@ __device__ void accept_scan(const Params& P, int b) {
     }
     tok_bad |= __ballot_sync(0xffffffffu, tbad);
     nf_bad |= __ballot_sync(0xffffffffu, fbad);
+    to_bad |= __ballot_sync(0xffffffffu, tmo);
     const unsigned rej = __ballot_sync(0xffffffffu, valid && !acc);
     if (n == k && rej) n = base + __ffs(rej) - 1;
   }
   // filtering runs over every row of the sequence, the bonus row included
-  if (P.filtering && ldcg_stat(P.ws.row_stat + rbase + 2 * k).status != SPEC_OK) nf_bad = 1;
+  if (P.filtering) {
+    const int bs = ldcg_stat(P.ws.row_stat + rbase + 2 * k).status;
+    if (bs != SPEC_OK) nf_bad = 1;
+    if (bs == SPEC_ERR_TIMEOUT) to_bad = 1;
+  }
   if (lane == 0) {
-    const int st = tok_bad ? SPEC_ERR_TOKEN : nf_bad ? SPEC_ERR_NONFINITE : SPEC_OK;
+    const int st = tok_bad ? SPEC_ERR_TOKEN : to_bad ? SPEC_ERR_TIMEOUT : nf_bad ? SPEC_ERR_NONFINITE : SPEC_OK;
     __stcg(reinterpret_cast<int2*>(P.ws.seq) + b, make_int2(n, st));
   }
 }
@@ -430,13 +440,14 @@ __device__ void greedy_match(const Params& P, int b) {
   const int k = P.k;
   const long long rbase = (long long)b * (k + 1);
   int n = k;
-  unsigned tok_bad = 0, nf_bad = 0;
+  unsigned tok_bad = 0, nf_bad = 0, to_bad = 0;
   for (int base = 0; base <= k; base += 32) {
     const int i = base + lane;
-    bool mism = false, tbad = false, fbad = false;
+    bool mism = false, tbad = false, fbad = false, tmo = false;
     if (i <= k) {
       const RowStat rs = ldcg_stat(P.ws.row_stat + rbase + i);
       fbad = rs.status != SPEC_OK;
+      tmo = rs.status == SPEC_ERR_TIMEOUT;
       if (i < k) {
         const int x = P.tokens[(size_t)b * k + i];
         tbad = x < 0 || x >= P.V;
@@ -445,6 +456,7 @@ __device__ void greedy_match(const Params& P, int b) {
     }
     tok_bad |= __ballot_sync(0xffffffffu, tbad);
     nf_bad |= __ballot_sync(0xffffffffu, fbad);
+    to_bad |= __ballot_sync(0xffffffffu, tmo);
     const unsigned mm = __ballot_sync(0xffffffffu, mism);
     if (n == k && mm) n = base + __ffs(mm) - 1;
   }
@@ -466,7 +478,7 @@ __device__ void greedy_match(const Params& P, int b) {
     tok_bad |= gbad;
     if (n < P.L && g[n] == an) gend = first_neg;
   }
-  const int st = tok_bad ? SPEC_ERR_TOKEN : nf_bad ? SPEC_ERR_NONFINITE : SPEC_OK;
+  const int st = tok_bad ? SPEC_ERR_TOKEN : to_bad ? SPEC_ERR_TIMEOUT : nf_bad ? SPEC_ERR_NONFINITE : SPEC_OK;
   int32_t* out = P.out_tokens + (size_t)b * P.out_w;
   const int32_t* x = P.tokens + (size_t)b * k;
   const int committed = write_committed(P, out, P.out_w, [&](int i) -> int {
@@ -522,9 +534,15 @@ __device__ void tree_walk(const Params& P, int b) {
     s_par[m] = (short)(ok_shape ? par : -1);
     s_dep[m] = (short)ok;
   }
-  for (int r = lane; r <= N; r += 32) fbad |= ldcg_stat(P.ws.row_stat + rbase + r).status != SPEC_OK;
+  int tmo = 0;
+  for (int r = lane; r <= N; r += 32) {
+    const int rs = ldcg_stat(P.ws.row_stat + rbase + r).status;
+    fbad |= rs != SPEC_OK;
+    tmo |= rs == SPEC_ERR_TIMEOUT;
+  }
   tbad = __any_sync(0xffffffffu, tbad);
   fbad = __any_sync(0xffffffffu, fbad);
+  tmo = __any_sync(0xffffffffu, tmo);
   __syncwarp();
   int best = -1, best_d = 0;
   if (lane == 0) {
@@ -539,7 +557,7 @@ __device__ void tree_walk(const Params& P, int b) {
   best = __shfl_sync(0xffffffffu, best, 0);
   best_d = __shfl_sync(0xffffffffu, best_d, 0);
   __syncwarp();
-  const int st = tbad ? SPEC_ERR_TOKEN : fbad ? SPEC_ERR_NONFINITE : SPEC_OK;
+  const int st = tbad ? SPEC_ERR_TOKEN : tmo ? SPEC_ERR_TIMEOUT : fbad ? SPEC_ERR_NONFINITE : SPEC_OK;
   int32_t* out = P.out_tokens + (size_t)b * (N + 1);
   for (int i = lane; i <= N; i += 32)
     if (st != SPEC_OK || i > best_d) out[i] = -1;
@@ -562,9 +580,10 @@ __device__ void finish_row(const Params& P, long long r, int b) {
   __threadfence();
   const float4* src = reinterpret_cast<const float4*>(P.ws.row_partial + r * P.nt);
   float m = -CUDART_INF_F, s = 0.f;
-  int ix = INT_MAX, bad = 0;
+  int ix = INT_MAX, bad = 0, tmo = 0;
   for (int t = lane; t < P.nt; t += 32) {
     const float4 p = __ldcg(src + t);
+    if (p.w != 0.f) { tmo = 1; continue; }          // a piece whose data never arrived
     if (p.x != p.x) { bad = 1; continue; }
     if constexpr (kMode == kStochastic) {
       const float M = fmaxf(m, p.x);
@@ -580,12 +599,14 @@ __device__ void finish_row(const Params& P, long long r, int b) {
     const float M = warp_max(m);
     s = warp_sum(rescale(s, m, M, P.c));
     bad = __any_sync(0xffffffffu, bad);
+    tmo = __any_sync(0xffffffffu, tmo);
     const bool finite = M > -CUDART_INF_F && M < CUDART_INF_F && s > 0.f && s < CUDART_INF_F;
-    st = RowStat{M, logf(s), INT_MAX, (bad || !finite) ? SPEC_ERR_NONFINITE : SPEC_OK};
+    st = RowStat{M, logf(s), INT_MAX, tmo ? SPEC_ERR_TIMEOUT : (bad || !finite) ? SPEC_ERR_NONFINITE : SPEC_OK};
   } else {
     warp_argmax(m, ix);
     bad = __any_sync(0xffffffffu, bad);
-    st = RowStat{m, 0.f, ix, bad ? SPEC_ERR_NONFINITE : SPEC_OK};
+    tmo = __any_sync(0xffffffffu, tmo);
+    st = RowStat{m, 0.f, ix, tmo ? SPEC_ERR_TIMEOUT : bad ? SPEC_ERR_NONFINITE : SPEC_OK};
   }
   if (kMode == kStochastic && P.filtering) {
     // the filter pass takes the row from here and runs the accept scan
@@ -681,6 +702,162 @@ __global__ void __launch_bounds__(kThreads, kRowPassMinCtas<T>) row_pass_kernel(
     end_piece<T, kMode>(P, r, b, t0, t1, part);
     __syncthreads();
     i += t1 - t0;
+  }
+}
+
+// ------------------------------------------------ row pass, bulk-copy ring ---
+//
+// For greedy and tree verification, when every row starts on a 16-byte
+// boundary, the row pass stages its data in shared memory with bulk copies.  A producer warp keeps kRingStages copies of
+// up to kRingBytes of the CTA's range in flight, each completing on its
+// stage's "full" barrier; the eight consumer warps fold a stage from shared
+// memory and release it on its "empty" barrier.  The bytes in flight per SM
+// are then set by the ring, not by how many loads a thread can hold in
+// registers.  Ranges, pieces, partials and the completion steps are those of
+// the register row pass above.
+constexpr int kRingStages = 3;
+constexpr int kRingBytes = 16384;
+constexpr int kRingThreads = kThreads + 32;   // eight consumer warps, one producer warp
+constexpr int kRingMinCtas = 4;
+constexpr double kRingMinBytes = 134217728.0;   // 128 MiB of rows
+
+struct RingSmem {
+  alignas(128) unsigned char buf[kRingStages][kRingBytes];
+  uint64_t full[kRingStages];
+  uint64_t empty[kRingStages];
+  int abort;   // a wait ran out: the rest of the range is marked as timed out
+};
+
+// Piece walk shared by the producer and the consumers: the CTA's tiles
+// [i, i1) of the virtual row list, cut at row ends.
+struct PieceWalk {
+  long long i, i1;
+  __device__ PieceWalk(const Params& P) {
+    const long long I = P.R * P.nt;
+    i = I * blockIdx.x / gridDim.x;
+    i1 = I * (blockIdx.x + 1) / gridDim.x;
+  }
+};
+
+template <typename T, int kMode>
+__global__ void __launch_bounds__(kRingThreads, kRingMinCtas) row_pass_ring(const Params P) {
+  extern __shared__ __align__(128) unsigned char dyn_smem[];
+  RingSmem& S = *reinterpret_cast<RingSmem*>(dyn_smem);
+  __shared__ BlockScratch sh;
+  // the sampling launch may be scheduled as this grid's CTAs retire; it waits
+  // for this grid's results before reading them
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kRingStages; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], kWarps);
+    }
+    fence_mbar_init();
+    S.abort = 0;
+  }
+  __syncthreads();
+
+  if (warp == kWarps) {
+    // producer: one lane issues the copies, kRingStages ahead of the consumers
+    if (lane != 0) return;
+    long long q = 0;
+    PieceWalk w(P);
+    while (w.i < w.i1 && !*(volatile int*)&S.abort) {
+      const long long r = w.i / P.nt;
+      const int t0 = (int)(w.i % P.nt);
+      const int t1 = (int)min((long long)P.nt, (long long)t0 + (w.i1 - w.i));
+      int b;
+      const unsigned char* row = reinterpret_cast<const unsigned char*>(row_ptr<T, kMode>(P, r, b));
+      const size_t x0 = (size_t)t0 * kPartTile * sizeof(T);
+      const size_t x1 = (size_t)min(P.V, t1 * kPartTile) * sizeof(T);
+      for (size_t x = x0; x < x1 && !S.abort; x += kRingBytes, ++q) {
+        const int s = (int)(q % kRingStages);
+        if (q >= kRingStages &&
+            !mbar_wait_bounded(&S.empty[s], (unsigned)((q / kRingStages) - 1) & 1u)) {
+          S.abort = 1;
+          break;
+        }
+        fence_proxy_async_smem();
+        const unsigned nb = (unsigned)min((size_t)kRingBytes, x1 - x);
+        mbar_arrive_tx(&S.full[s], nb);
+        bulk_copy_g2s(S.buf[s], row + x, nb, &S.full[s]);
+      }
+      w.i += t1 - t0;
+    }
+    if (*(volatile int*)&S.abort) {
+      // leave no copy in flight into this CTA's shared memory (bounded)
+      for (long long x = q - 1; x >= 0 && x >= q - kRingStages; --x)
+        mbar_wait_bounded(&S.full[x % kRingStages], (unsigned)(x / kRingStages) & 1u);
+    }
+    return;
+  }
+
+  // consumers: fold each stage, release it, and end each piece as the register
+  // row pass does
+  constexpr int kVec = Vec<T>::n;
+  constexpr int kPer = kRingBytes / 16 / kThreads;   // 16-byte vectors per thread per full stage
+  long long q = 0;
+  PieceWalk w(P);
+  while (w.i < w.i1) {
+    const long long r = w.i / P.nt;
+    const int t0 = (int)(w.i % P.nt);
+    const int t1 = (int)min((long long)P.nt, (long long)t0 + (w.i1 - w.i));
+    int b;
+    row_ptr<T, kMode>(P, r, b);
+    const int e0 = t0 * kPartTile, e1 = min(P.V, t1 * kPartTile);
+    constexpr int kStageElems = kRingBytes / (int)sizeof(T);
+    LseAcc lacc;
+    ArgmaxAcc aacc;
+    if constexpr (kMode == kStochastic) lacc.init(P.c);
+    else aacc.init();
+    for (int ex = e0; ex < e1; ex += kStageElems, ++q) {
+      const int s = (int)(q % kRingStages);
+      if (!*(volatile int*)&S.abort && !mbar_wait_bounded(&S.full[s], (unsigned)(q / kRingStages) & 1u))
+        S.abort = 1;
+      if (*(volatile int*)&S.abort) continue;
+      const uint4* sv = reinterpret_cast<const uint4*>(S.buf[s]);
+      const int nvec = min(kStageElems, e1 - ex) / kVec;
+      if (nvec == kPer * kThreads) {
+        uint4 v[kPer];
+        int idx[kPer];
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+          v[u] = sv[u * kThreads + threadIdx.x];
+          idx[u] = ex + (u * kThreads + threadIdx.x) * kVec;
+        }
+        if constexpr (kMode == kStochastic) lacc.template vec<T, kPer>(v, idx);
+        else aacc.template vec<T, kPer>(v, idx);
+      } else {
+        for (int j = threadIdx.x; j < nvec; j += kThreads) {
+          uint4 v[1] = {sv[j]};
+          int idx[1] = {ex + j * kVec};
+          if constexpr (kMode == kStochastic) lacc.template vec<T, 1>(v, idx);
+          else aacc.template vec<T, 1>(v, idx);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.empty[s]);
+    }
+    // after the reduction's barriers every skipped stage has set the flag: a
+    // piece that lost data is marked timed out
+    float4 part;
+    if constexpr (kMode == kStochastic) {
+      float m = lacc.m, sum = lacc.sum();
+      int bad = lacc.bad;
+      block_lse_flag<true>(m, sum, bad, P.c, sh);
+      part = make_float4(bad ? CUDART_NAN_F : m, sum, __int_as_float(INT_MAX), 0.f);
+    } else {
+      float v = aacc.bv;
+      int ix = aacc.bi, bad = aacc.bad;
+      block_argmax_flag<true>(v, ix, bad, sh);
+      part = make_float4(bad ? CUDART_NAN_F : v, 0.f, __int_as_float(ix), 0.f);
+    }
+    if (*(volatile int*)&S.abort) part.w = 1.f;
+    // warp 0 stores the partial (and merges a completed row) while the other
+    // consumer warps go on: the next reduction's barriers order the scratch
+    end_piece<T, kMode>(P, r, b, t0, t1, part);
+    w.i += t1 - t0;
   }
 }
 
@@ -1654,11 +1831,23 @@ static int launch(Params& P, cudaStream_t stream, const spec_verify_aux* aux) {
                                    : cudaSuccess;
   };
   const long long items = P.R * P.nt;
-  const int ctas = resident_ctas(reinterpret_cast<const void*>(&row_pass_kernel<T, kMode>));
+  // greedy and tree rows on 16-byte boundaries, over more than L2 holds, are
+  // staged by bulk copies (measured: 30.6 vs 33.2 us on 64 x 9 rows of 128256
+  // bf16; on 66 MB of rows 22.0 vs 21.1 us, so smaller batches keep the
+  // register path); the stochastic pass, with an exponential per element,
+  // keeps more warps per SM with the register path (51.0 vs 55.0 us on 64 x 16
+  // rows), as do unaligned rows
+  const bool ring = kMode != kStochastic && aligned(P.target, 16) && ((size_t)P.V * sizeof(T)) % 16 == 0 &&
+                    (double)P.R * (double)P.V * sizeof(T) >= kRingMinBytes;
+  const void* rp = ring ? reinterpret_cast<const void*>(&row_pass_ring<T, kMode>)
+                        : reinterpret_cast<const void*>(&row_pass_kernel<T, kMode>);
+  const size_t rsmem = ring ? sizeof(RingSmem) : 0;
+  const int ctas = resident_ctas(rp, rsmem, ring ? kRingThreads : kThreads);
   if (ctas <= 0) return SPEC_ERR_CUDA;
   const int grid = (int)(items < ctas ? items : ctas);
   if (rec(0) != cudaSuccess) return SPEC_ERR_CUDA;
-  row_pass_kernel<T, kMode><<<grid, kThreads, 0, stream>>>(P);
+  if (ring) row_pass_ring<T, kMode><<<grid, kRingThreads, rsmem, stream>>>(P);
+  else row_pass_kernel<T, kMode><<<grid, kThreads, 0, stream>>>(P);
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   if (rec(1) != cudaSuccess) return SPEC_ERR_CUDA;
   if constexpr (kMode == kStochastic) {
