@@ -277,8 +277,14 @@ def run_ours(args):
     for i in range(nk):
         step(i, ev[i])
     torch.cuda.synchronize()
-    row_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    row_t = [e[0].elapsed_time(e[1]) for e in ev]
+    call_t = [e[0].elapsed_time(e[3]) for e in ev]
+    row_ms = statistics.mean(row_t)
     samp_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
+
+    def pct(xs):
+        q = np.percentile(np.asarray(xs) * 1e3, [10, 50, 90])
+        return {"p10_us": float(q[0]), "p50_us": float(q[1]), "p90_us": float(q[2])}
     rows_per_step = B * (K + 1)
     value = world * rows_per_step * args.steps / elapsed
 
@@ -335,6 +341,7 @@ def run_ours(args):
                        "step_bytes": step_bytes, "residual_bytes": resid_bytes,
                        "step_hbm_gbs": step_bytes / (elapsed / args.steps) / 1e9,
                        "row_pass_ms": row_ms, "sample_ms": samp_ms,
+                       "row_pass_us_percentiles": pct(row_t), "evented_call_us_percentiles": pct(call_t),
                        "sample_bytes_l2_or_hbm": resid_bytes},
             "roofline": {"bound": "hbm", "kernel": "row_pass_kernel", "achieved": achieved, "peak": peak,
                          "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
