@@ -76,6 +76,13 @@ __device__ __forceinline__ uint32_t bf16x2_nanmax(uint32_t a, uint32_t b) {
   return d;
 }
 
+// Packed bf16x2 min (operands are never NaN where it is used).
+__device__ __forceinline__ uint32_t bf16x2_min(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("min.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
 // bf16 -> fp32 is exact: the 16 bits become the top half of the fp32 word.
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }

@@ -815,7 +815,8 @@ __global__ void __launch_bounds__(kRingThreads, kRingMinCtas) row_pass_ring(cons
       const int s = (int)(q % kRingStages);
       if (!*(volatile int*)&S.abort && !mbar_wait_bounded(&S.full[s], (unsigned)(q / kRingStages) & 1u))
         S.abort = 1;
-      if (*(volatile int*)&S.abort) continue;
+      // one decision per warp, so that every lane reaches the same __syncwarp
+      if (__any_sync(0xffffffffu, *(volatile int*)&S.abort != 0)) continue;
       const uint4* sv = reinterpret_cast<const uint4*>(S.buf[s]);
       const int nvec = min(kStageElems, e1 - ex) / kVec;
       if (nvec == kPer * kThreads) {
@@ -951,6 +952,7 @@ struct FilterScratch {
   unsigned long long massq[kHistBins];   // fixed-point sums, turned into `mass` after a pass
   uint32_t wc[kWarps];
   float wm[kWarps];
+  uint4 vq[kWarps][32];                  // per warp: 16-byte vectors that need the per-id test
   int sel_bin;
   uint32_t sel_cnt_above, sel_cnt_bin, total_cnt;
   float sel_mass_above, sel_mass_bin;
@@ -1094,10 +1096,11 @@ struct DistAcc {
   const Windows* W;
   int win;
   uint32_t tail_cnt;
+  float a0, b0;       // window 0's map, held in registers
   __device__ __forceinline__ void elem(float x) {
     if (win == 0) {
       // the common pass: one FMA and a compare for an id far below the max
-      const float s = fmaf(-x, W->a[0], W->b[0]);
+      const float s = fmaf(-x, a0, b0);
       if (!(s < (float)(kDistBins - 1))) {             // the tail, or -inf (s = +inf)
         if (x > -CUDART_INF_F && (key_min == 0u || Keys<T>::of(x) >= key_min)) ++tail_cnt;
         return;
@@ -1122,9 +1125,44 @@ struct DistAcc {
   template <typename TT, int U>
   __device__ __forceinline__ void vec(const uint4 (&v)[U], const int (&)[U]) {
 #pragma unroll
-    for (int u = 0; u < U; ++u)
+    for (int u = 0; u < U; ++u) {
+      // window 0 without a key floor: a vector whose largest logit lies below
+      // the window and which holds no -inf is all tail (the window position is
+      // non-increasing in the logit, so this is the per-id test's answer).
+      // The other vectors go to the warp's queue, and the warp's lanes share
+      // their ids out, so the per-id test runs with every lane busy.  Only
+      // scan_segment's full batches (U == kUnroll) come here: every thread of
+      // the CTA takes part in them, as the warp-wide ballot and syncs need; its
+      // remainder loop, where a warp may be partly idle, takes the per-id test.
+      if (U == kUnroll && win == 0 && key_min == 0u) {
+        float hi, lo;
+        if constexpr (sizeof(T) == 2) {
+          const uint32_t mx = bf16x2_nanmax(bf16x2_nanmax(v[u].x, v[u].y), bf16x2_nanmax(v[u].z, v[u].w));
+          const uint32_t mn = bf16x2_min(bf16x2_min(v[u].x, v[u].y), bf16x2_min(v[u].z, v[u].w));
+          hi = fmaxf(bf16_lo(mx), bf16_hi(mx));
+          lo = fminf(bf16_lo(mn), bf16_hi(mn));
+        } else {
+          hi = fmaxf(fmaxf(__uint_as_float(v[u].x), __uint_as_float(v[u].y)),
+                     fmaxf(__uint_as_float(v[u].z), __uint_as_float(v[u].w)));
+          lo = fminf(fminf(__uint_as_float(v[u].x), __uint_as_float(v[u].y)),
+                     fminf(__uint_as_float(v[u].z), __uint_as_float(v[u].w)));
+        }
+        const bool all_tail = lo > -CUDART_INF_F && !(fmaf(-hi, a0, b0) < (float)(kDistBins - 1));
+        if (all_tail) tail_cnt += Vec<T>::n;
+        const int lane = threadIdx.x & 31;
+        const unsigned slow = __ballot_sync(0xffffffffu, !all_tail);
+        if (!slow) continue;
+        uint4* q = S->vq[threadIdx.x >> 5];
+        if (!all_tail) q[__popc(slow & ((1u << lane) - 1u))] = v[u];
+        __syncwarp();
+        const int n = __popc(slow) * Vec<T>::n;
+        for (int i = lane; i < n; i += 32) elem(Vec<T>::at(q[i / Vec<T>::n], i % Vec<T>::n));
+        __syncwarp();                    // the queue is refilled by the next vector
+        continue;
+      }
 #pragma unroll
       for (int e = 0; e < Vec<T>::n; ++e) elem(Vec<T>::at(v[u], e));
+    }
   }
   __device__ __forceinline__ void scalar(float x, int) { elem(x); }
 };
@@ -1143,7 +1181,7 @@ __device__ bool find_threshold(const T* row, const Params& P, const RowStat& rs,
   for (; win < kWindows; ++win) {
     clear_hist(S, kDistBins);
     __syncthreads();
-    DistAcc<T> da{&S, key_min, P.c, rs.m * P.c, &W, win, 0u};
+    DistAcc<T> da{&S, key_min, P.c, rs.m * P.c, &W, win, 0u, W.a[0], W.b[0]};
     scan_segment<T>(row, 0, P.V, da);
     const uint32_t tc = __reduce_add_sync(0xffffffffu, da.tail_cnt);
     if ((threadIdx.x & 31) == 0 && tc) atomicAdd(&S.cnt[0], tc);
@@ -1228,7 +1266,7 @@ __device__ bool find_threshold(const T* row, const Params& P, const RowStat& rs,
 // One CTA per row: its threshold and kept mass; the CTA that filters a
 // sequence's last row runs the sequence's accept scan on the filtered rows.
 template <typename T>
-__global__ void __launch_bounds__(kThreads) filter_kernel(const Params P) {
+__global__ void __launch_bounds__(kThreads, 6) filter_kernel(const Params P) {
   __shared__ FilterScratch S;
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // the row pass's statistics must be visible
