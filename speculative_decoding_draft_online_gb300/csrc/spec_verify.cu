@@ -708,13 +708,17 @@ __global__ void __launch_bounds__(kThreads, kRowPassMinCtas<T>) row_pass_kernel(
 // ------------------------------------------------ row pass, bulk-copy ring ---
 //
 // For greedy and tree verification, when every row starts on a 16-byte
-// boundary, the row pass stages its data in shared memory with bulk copies.  A producer warp keeps kRingStages copies of
-// up to kRingBytes of the CTA's range in flight, each completing on its
-// stage's "full" barrier; the eight consumer warps fold a stage from shared
-// memory and release it on its "empty" barrier.  The bytes in flight per SM
-// are then set by the ring, not by how many loads a thread can hold in
-// registers.  Ranges, pieces, partials and the completion steps are those of
-// the register row pass above.
+// boundary, the row pass stages its data in shared memory with bulk copies.
+// A producer warp keeps kRingStages copies of up to kRingBytes of the CTA's
+// range in flight, each completing on its stage's "full" barrier; the eight
+// consumer warps fold a stage from shared memory and release it on its
+// "empty" barrier.  The bytes in flight per SM are then set by the ring, not
+// by how many loads a thread can hold in registers.  Ranges, pieces, partials
+// and the completion steps are those of the register row pass above.  Every
+// wait is bounded: a wait that runs out stops the producer, marks the CTA's
+// remaining pieces as timed out (their rows and sequences get
+// SPEC_ERR_TIMEOUT) and, before the CTA leaves, the producer waits (bounded)
+// for the copies it has in flight.
 constexpr int kRingStages = 3;
 constexpr int kRingBytes = 16384;
 constexpr int kRingThreads = kThreads + 32;   // eight consumer warps, one producer warp
