@@ -72,7 +72,8 @@ enum spec_status {
   SPEC_ERR_TOKEN = -3,        /* (device) token id outside [0, V) or bad tree parent          */
   SPEC_ERR_NONFINITE = -4,    /* (device) NaN / +inf logit, or a row with no finite logit     */
   SPEC_ERR_UNSUPPORTED = -5,  /* e.g. stochastic tree verification, k or N above the limit    */
-  SPEC_ERR_TIMEOUT = -6,      /* reserved: a bounded device wait gave up                      */
+  SPEC_ERR_TIMEOUT = -6,      /* (device) a bounded wait on a bulk copy gave up (1 s); the    */
+                              /*   sequences whose rows it held get -1 outputs                 */
   SPEC_ERR_CUDA = -7,         /* a CUDA runtime call failed (launch, event record)           */
   SPEC_ERR_WORKSPACE = -8     /* workspace NULL, misaligned or smaller than required          */
 };
