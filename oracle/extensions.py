@@ -191,7 +191,12 @@ def filter_row(x: np.ndarray, temperature: float, top_k: int, top_p: float) -> R
         for v in values:
             grp = float(w[base & (x == v)].sum())
             if cum + grp >= target:
-                margin = min(cum + grp - target, target - cum) / mk
+                # the chosen value moves when the target crosses either end of
+                # its group's cumulative mass: the upper end (cum + grp) or the
+                # lower end (cum), which only a group after the first has --
+                # no top_p > 0 falls below a cumulative mass of 0
+                upper = cum + grp - target
+                margin = (min(upper, target - cum) if cum > 0 else upper) / mk
                 tau = max(tau, float(v))
                 break
             cum += grp

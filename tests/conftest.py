@@ -27,3 +27,15 @@ def read_golden(name):
 @pytest.fixture
 def golden():
     return read_golden
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Record how many stochastic positions the parity tests compared and how
+    many of those the margin rule excused (the bound is under 0.01 %)."""
+    mod = sys.modules.get("tests.gpu_parity")
+    if mod is None or mod.SESSION.rows == 0:
+        return
+    t = mod.SESSION
+    terminalreporter.write_line(
+        f"stochastic parity: {t.rows} positions in {t.sequences} sequences compared, "
+        f"{t.margin_rows} excused by the margin rule ({100.0 * t.margin_rows / t.rows:.4f} %)")

@@ -42,8 +42,20 @@ class Tally:
         self.sequences += other.sequences
 
 
+# every comparison of the session, printed in pytest's terminal summary
+SESSION = Tally()
+
+
 def compare_stochastic(ref, out: np.ndarray, n: np.ndarray, status: np.ndarray, k: int) -> Tally:
-    """Sequence-by-sequence comparison with the margin rule; raises on a real mismatch."""
+    """Sequence-by-sequence comparison with the margin rule; raises on a real mismatch.
+
+    The returned tally is also added to SESSION."""
+    tally = _compare(ref, out, n, status, k)
+    SESSION.add(tally)
+    return tally
+
+
+def _compare(ref, out: np.ndarray, n: np.ndarray, status: np.ndarray, k: int) -> Tally:
     tally = Tally()
     B = out.shape[0]
     for b in range(B):

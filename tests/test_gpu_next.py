@@ -182,13 +182,6 @@ def test_guided_bad_guide_id(sv):
     np.testing.assert_array_equal(out.cpu().numpy()[ok], ref.out_tokens[ok])
 
 
-def test_margin_rows_under_one_in_ten_thousand():
-    """The stochastic positions of this file, under the same 0.01 % bound."""
-    if TALLY.rows < 10_000:
-        pytest.skip(f"only {TALLY.rows} positions compared in this run (a subset was selected)")
-    assert TALLY.margin_rows < 1e-4 * TALLY.rows, TALLY
-
-
 # ---------------------------------------------------------- top-k / top-p ---
 
 def _filtered(sv, w, seed, top_k, top_p, target=None, draft=None):
@@ -252,3 +245,13 @@ def test_filtering_is_ignored_in_greedy_mode(sv):
     o2, n2, _ = sv.verify_ex(t, None, x, 0.0, 0, top_k=3, top_p=0.5, committed=True)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(n1, n2)
+
+
+def test_margin_rows_under_one_in_ten_thousand():
+    """The stochastic positions of this file (every test above, the filtered
+    ones included), under the same 0.01 % bound.  Kept last: pytest runs a
+    file's tests in order."""
+    if TALLY.rows < 10_000:
+        pytest.skip(f"only {TALLY.rows} positions compared in this run (a subset was selected)")
+    print(f"excused {TALLY.margin_rows} of {TALLY.rows} positions")
+    assert TALLY.margin_rows < 1e-4 * TALLY.rows, TALLY
