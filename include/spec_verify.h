@@ -40,10 +40,15 @@
  *
  * Workspace: a caller-owned device buffer of spec_workspace_size() bytes.  It
  * must be zero-filled once before its first use (spec_workspace_init or any
- * memset).  A call returns the completion counters inside it to zero; when a
- * workspace is used with sizes other than those of its previous call, the
- * library clears it first (one cudaMemsetAsync on the call's stream).  Two
- * calls that may overlap in time must not share a workspace.
+ * memset).  A call returns the completion counters inside it to zero.  Where
+ * they sit depends on (B, k or N, V), so the library clears their region first
+ * (one cudaMemsetAsync of a few KB on the call's stream) when a workspace is
+ * used with sizes other than those of the previous eager call on it.  A call
+ * queued under stream capture always records that clear into the graph, so
+ * every replay starts from zeroed counters, and once a workspace has been used
+ * under capture every later eager call on it clears too (the library cannot
+ * tell when the graph's replays run).  Two calls that may overlap in time must
+ * not share a workspace.
  *
  * Errors: argument errors are detected on the host and returned before any
  * launch (nothing is written).  Conditions only visible in the data -- a NaN
@@ -230,9 +235,12 @@ int spec_random(uint64_t seed, int b, int j, int V, float* gumbel_u, float* gumb
  *   The first call on each device looks up the array's device address (once,
  *   with that device current); make that first call before any stream capture.
  *   All calls share the one array per device and it keeps the previous call's
- *   contents (the library clears what must start at zero), so calls whose work
- *   may overlap on the GPU -- other streams, other host threads -- race with
- *   each other: order them on one stream.
+ *   contents (the library clears what must start at zero, as for a workspace:
+ *   a call captured into a graph clears the counters on every replay, and
+ *   after any capture every eager call clears them too), so calls whose work
+ *   may overlap on the GPU -- other streams, other host threads, a graph
+ *   replay next to an eager call -- race with each other: order them on one
+ *   stream.
  */
 #define SPEC_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
 int spec_verify_noalloc(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,

@@ -49,6 +49,7 @@
 #include <mutex>
 #include <type_traits>
 #include <unordered_map>
+#include <unordered_set>
 
 #include "spec_device.cuh"
 #include "spec_verify.h"
@@ -1781,8 +1782,12 @@ __global__ void random_kernel(uint2 key, int b, int j, int V, float* gu, float* 
 
 // --------------------------------------------------------------- host side ---
 
+// The workspace: first the counters that must read zero when a call starts
+// (one contiguous region, so clearing them is one small memset), then the
+// records every call writes before it reads them.
 struct Layout {
-  size_t row_partial, row_cnt, row_stat, row_filter, seq_cnt, seq, samp_partial, samp_cnt, samp_floor, total;
+  size_t row_cnt, seq_cnt, samp_cnt, samp_floor, counters_end;   // the zeroed region [0, counters_end)
+  size_t row_partial, row_stat, row_filter, seq, samp_partial, total;
   int nt;
   long long rmax;
 };
@@ -1794,17 +1799,18 @@ static bool make_layout(int B, int k, int V, Layout& L) {
   L.nt = (V + kPartTile - 1) / kPartTile;
   L.rmax = (long long)B * (long long)(2 * k + 1);   // the most rows any mode takes statistics of
   size_t off = 0;
-  auto take = [&](size_t bytes) { const size_t o = off; off = align_up(off + bytes, 256); return o; };
-  L.row_partial = take((size_t)L.rmax * L.nt * sizeof(Partial));
-  L.row_cnt = take((size_t)L.rmax * sizeof(unsigned));
-  L.row_stat = take((size_t)L.rmax * sizeof(RowStat));
-  L.row_filter = take((size_t)L.rmax * sizeof(float2));
-  L.seq_cnt = take((size_t)B * sizeof(unsigned));
-  L.seq = take((size_t)B * sizeof(SeqState));
-  L.samp_partial = take((size_t)B * L.nt * sizeof(float2));
-  L.samp_cnt = take((size_t)B * sizeof(unsigned));
-  L.samp_floor = take((size_t)B * sizeof(unsigned));
-  L.total = off;
+  auto take = [&](size_t bytes, size_t a) { off = align_up(off, a); const size_t o = off; off += bytes; return o; };
+  L.row_cnt = take((size_t)L.rmax * sizeof(unsigned), 4);
+  L.seq_cnt = take((size_t)B * sizeof(unsigned), 4);
+  L.samp_cnt = take((size_t)B * sizeof(unsigned), 4);
+  L.samp_floor = take((size_t)B * sizeof(unsigned), 4);
+  L.counters_end = off;
+  L.row_partial = take((size_t)L.rmax * L.nt * sizeof(Partial), 256);
+  L.row_stat = take((size_t)L.rmax * sizeof(RowStat), 256);
+  L.row_filter = take((size_t)L.rmax * sizeof(float2), 256);
+  L.seq = take((size_t)B * sizeof(SeqState), 256);
+  L.samp_partial = take((size_t)B * L.nt * sizeof(float2), 256);
+  L.total = align_up(off, 256);
   return true;
 }
 
@@ -1825,23 +1831,44 @@ static Workspace bind(void* base, const Layout& L) {
 
 static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// The completion counters sit at layout-dependent offsets, and a call returns
-// only them to zero.  A workspace used with new sizes is therefore cleared
-// first; the library remembers the sizes each workspace last served.
+// Every call returns the counters it used to zero, but where they sit depends
+// on the sizes, so a workspace that served other sizes holds other records
+// there.  The counter region is then cleared first (one cudaMemsetAsync on the
+// call's stream).  The library remembers, per workspace, the sizes of the last
+// call queued eagerly on it and skips the clear when they repeat.  That record
+// follows the host's queueing order, not the GPU's execution order, which a
+// captured graph breaks (its replays run whenever the caller launches them):
+// so a call queued under stream capture always records the clear into the
+// graph (each replay clears), and a workspace once used under capture is
+// cleared by every later eager call too.
+struct Sizes {
+  int B, k, V;
+  bool operator==(const Sizes& o) const { return B == o.B && k == o.k && V == o.V; }
+};
+
 static int prepare_workspace(void* ws, const Layout& L, int B, int k, int V, cudaStream_t stream) {
   static std::mutex mu;
-  static std::unordered_map<uintptr_t, uint64_t> last;
-  const uint64_t sig = ((uint64_t)(uint32_t)V << 32) ^ ((uint64_t)(uint32_t)B << 12) ^ (uint64_t)(uint32_t)k ^
-                       ((uint64_t)(uint32_t)k << 44);
+  static std::unordered_map<uintptr_t, Sizes> last;       // eager calls on never-captured workspaces
+  static std::unordered_set<uintptr_t> captured;          // workspaces used under stream capture
+  const uintptr_t key = reinterpret_cast<uintptr_t>(ws);
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  const bool known = cudaStreamIsCapturing(stream, &cs) == cudaSuccess;
+  bool clear = true;
   {
     std::lock_guard<std::mutex> lock(mu);
-    auto it = last.find(reinterpret_cast<uintptr_t>(ws));
-    if (it != last.end() && it->second == sig) return SPEC_OK;
-    last[reinterpret_cast<uintptr_t>(ws)] = sig;
+    if (!known || cs != cudaStreamCaptureStatusNone) {
+      captured.insert(key);
+      last.erase(key);
+    } else if (!captured.count(key)) {
+      auto it = last.find(key);
+      clear = !(it != last.end() && it->second == Sizes{B, k, V});
+      last[key] = Sizes{B, k, V};
+    }
   }
-  if (cudaMemsetAsync(ws, 0, L.total, stream) != cudaSuccess) {
+  if (!known) (void)cudaGetLastError();
+  if (clear && cudaMemsetAsync(ws, 0, L.counters_end, stream) != cudaSuccess) {
     std::lock_guard<std::mutex> lock(mu);
-    last.erase(reinterpret_cast<uintptr_t>(ws));
+    last.erase(key);
     return SPEC_ERR_CUDA;
   }
   return SPEC_OK;
@@ -2201,9 +2228,11 @@ extern "C" int spec_verify_noalloc(const void* target_logits, const void* draft_
   const int rc = sv::noalloc_scratch_address(&scratch);
   if (rc != SPEC_OK) return rc;
   // The scratch keeps whatever the previous call left in it.  The counters
-  // that must start at zero are returned to zero by every call, and
-  // spec_verify_ex clears the region first whenever the sizes differ from
-  // those of the previous call on this scratch.
+  // that must start at zero are returned to zero by every call.  spec_verify_ex
+  // clears their region first when the sizes differ from those of the previous
+  // eager call on this scratch, on every call queued under stream capture (the
+  // clear becomes part of the graph), and on every call once the scratch has
+  // been used under capture.
   return spec_verify_ex(target_logits, draft_logits, draft_tokens, B, k, V, dtype, temperature, seed, out_tokens,
                         out_n_accepted, scratch, sv::kNoAllocScratchBytes, cuda_stream, nullptr);
 }

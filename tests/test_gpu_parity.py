@@ -235,6 +235,44 @@ def test_workspace_reuse_and_determinism(sv):
         np.testing.assert_array_equal(g[0].cpu().numpy(), gref.out_tokens)
 
 
+def test_workspace_reuse_across_graph_capture(sv):
+    """One workspace serves eager calls at one size and a graph captured at
+    another, interleaved on one stream; every result equals a fresh
+    workspace's (the counters are cleared wherever consecutive executions may
+    differ in size, whatever order the replays run in)."""
+    ws = sv.workspace(64, 16, 200000, sv.SPEC_BF16, "cuda")
+    a = wl.gaussian_pair(6, 5, 3333, wl.BF16, 0.8, seed=3, sigma_t=3.0, sigma_d=1.0)
+    g = wl.c4(0.7, seed=4, B=5, k=9, V=4000)
+    a_t, a_d, a_x = to_device(a.target, a.dtype), to_device(a.draft, a.dtype), tokens_to_device(a.tokens)
+    g_t, g_x = to_device(g.target, g.dtype), tokens_to_device(g.tokens)
+    a_ref = [r.clone() for r in sv.verify(a_t, a_d, a_x, 0.8, 7)]
+    g_ref = [r.clone() for r in sv.verify(g_t, None, g_x, 0.0)]
+
+    def eager_a():
+        out = sv.verify(a_t, a_d, a_x, 0.8, 7, ws=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(out[0], a_ref[0]) and torch.equal(out[1], a_ref[1])
+
+    eager_a()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        g_out = sv.verify(g_t, None, g_x, 0.0, ws=ws)
+    torch.cuda.synchronize()
+    for step in ("eager", "replay", "a", "replay", "replay", "a", "eager", "replay"):
+        if step == "a":
+            eager_a()
+            continue
+        if step == "eager":
+            out = sv.verify(g_t, None, g_x, 0.0, ws=ws)
+        else:
+            g_out[0].fill_(-7)
+            graph.replay()
+            out = g_out
+        torch.cuda.synchronize()
+        assert torch.equal(out[0], g_ref[0]) and torch.equal(out[1], g_ref[1]), step
+
+
 def test_side_stream(sv):
     w = wl.gaussian_pair(4, 4, 5000, wl.BF16, 1.0, seed=21, sigma_t=3.0, sigma_d=1.0)
     s = torch.cuda.Stream()
