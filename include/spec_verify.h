@@ -275,6 +275,20 @@ int spec_verify_guided(const void* target_logits, const int32_t* draft_tokens, c
                        int32_t* out_tokens, int32_t* out_n_accepted, int32_t* out_n_committed,
                        int32_t* status, void* workspace, size_t workspace_bytes, void* cuda_stream);
 
+/*
+ * spec_test_force_stage_timeouts -- test hook (since ABI 1.3), off by default.
+ *   on != 0: from the next call on, every wait of a bulk-copy stage (the ring
+ *   row pass of large greedy and tree batches, and the sampling pass of
+ *   stochastic calls on 16-byte aligned rows) gives up at once, as a wait does
+ *   when a copy has not landed within its 1 s limit: the affected sequences get
+ *   SPEC_ERR_TIMEOUT and -1 outputs, and before a CTA exits it still waits
+ *   (bounded) for the copies it has in flight.  on == 0 restores normal waits.
+ *   The setting is process-wide and read when a call is queued; it is meant
+ *   for tests of the timeout path, never for production calls.  Returns the
+ *   previous setting.
+ */
+int spec_test_force_stage_timeouts(int on);
+
 /* Human-readable name of a status code (static storage). */
 const char* spec_strerror(int status);
 

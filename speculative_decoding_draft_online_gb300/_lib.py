@@ -40,7 +40,7 @@ class _Aux(ctypes.Structure):
                 ("top_k", ctypes.c_int32), ("top_p", ctypes.c_float)]
 
 
-ABI_MIN = (1 << 16) | 2
+ABI_MIN = (1 << 16) | 3
 
 
 def _load():
@@ -68,6 +68,8 @@ def _load():
     L.spec_strerror.restype = ctypes.c_char_p
     L.spec_abi_version.argtypes = []
     L.spec_abi_version.restype = i32
+    L.spec_test_force_stage_timeouts.argtypes = [i32]
+    L.spec_test_force_stage_timeouts.restype = i32
     if L.spec_abi_version() < ABI_MIN or (L.spec_abi_version() >> 16) != (ABI_MIN >> 16):
         raise ImportError(f"{LIB_PATH} has ABI {L.spec_abi_version():#x}, this binding needs {ABI_MIN:#x}")
     return L
@@ -281,3 +283,9 @@ def random_stream(seed: int, b: int, j: int, V: int, device="cuda", stream=None)
     if rc != SPEC_OK:
         raise SpecError(rc, "spec_random")
     return u, g, a
+
+
+def force_stage_timeouts(on: bool) -> bool:
+    """Test hook: make every bulk-copy stage wait of later calls give up at once
+    (spec_test_force_stage_timeouts).  Returns the previous setting."""
+    return bool(lib.spec_test_force_stage_timeouts(1 if on else 0))

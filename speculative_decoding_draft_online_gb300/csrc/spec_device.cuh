@@ -292,6 +292,32 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity
   return true;
 }
 
+// As mbar_wait_bounded, for one warp waiting on behalf of a CTA whose other
+// warps sleep at a barrier: between polls the warp sleeps (32 ns, doubling up
+// to 512 ns), so that it takes no issue slots from warps that compute.
+__device__ __forceinline__ bool mbar_wait_sleepy(uint64_t* bar, unsigned parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = global_ns();
+  unsigned ns = 32;
+  while (!mbar_try_wait(bar, parity)) {
+    __nanosleep(ns);
+    ns = ns < 512 ? 2 * ns : 512;
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
+  return true;
+}
+
+// As mbar_wait_bounded, but also gives up (false) once *stop is nonzero.
+__device__ __forceinline__ bool mbar_wait_bounded_unless(uint64_t* bar, unsigned parity, const int* stop) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = global_ns();
+  while (!mbar_try_wait_suspend(bar, parity, 20000u)) {
+    if (*(const volatile int*)stop) return false;
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
+  return true;
+}
+
 // One bulk copy global -> this CTA's shared memory; completion is counted on `bar`.
 // Both addresses 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, unsigned bytes, uint64_t* bar) {

@@ -42,6 +42,7 @@
 // whichever CTA finishes last.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -131,6 +132,7 @@ struct Params {
   int filtering;               // stochastic rows go through top-k / top-p
   int top_k;                   // 0: off
   float top_p;                 // 0 or 1: off
+  int force_timeout;           // test hook: every bulk-copy stage wait gives up at once
   Workspace ws;
 };
 
@@ -778,8 +780,9 @@ __global__ void __launch_bounds__(kRingThreads, kRingMinCtas) row_pass_ring(cons
       const size_t x1 = (size_t)min(P.V, t1 * kPartTile) * sizeof(T);
       for (size_t x = x0; x < x1 && !S.abort; x += kRingBytes, ++q) {
         const int s = (int)(q % kRingStages);
+        // a consumer that gave up releases no stage: stop waiting when it says so
         if (q >= kRingStages &&
-            !mbar_wait_bounded(&S.empty[s], (unsigned)((q / kRingStages) - 1) & 1u)) {
+            !mbar_wait_bounded_unless(&S.empty[s], (unsigned)((q / kRingStages) - 1) & 1u, &S.abort)) {
           S.abort = 1;
           break;
         }
@@ -818,7 +821,8 @@ __global__ void __launch_bounds__(kRingThreads, kRingMinCtas) row_pass_ring(cons
     else aacc.init();
     for (int ex = e0; ex < e1; ex += kStageElems, ++q) {
       const int s = (int)(q % kRingStages);
-      if (!*(volatile int*)&S.abort && !mbar_wait_bounded(&S.full[s], (unsigned)(q / kRingStages) & 1u))
+      if (!*(volatile int*)&S.abort &&
+          (P.force_timeout || !mbar_wait_bounded(&S.full[s], (unsigned)(q / kRingStages) & 1u)))
         S.abort = 1;
       // one decision per warp, so that every lane reaches the same __syncwarp
       if (__any_sync(0xffffffffu, *(volatile int*)&S.abort != 0)) continue;
@@ -1349,6 +1353,19 @@ __device__ __forceinline__ bool may_reach(float u, float h, float floor) {
   return u >= __expf(-__expf(-need)) * (1.0f - 3e-5f);
 }
 
+// The smallest value of w >> 9 for a Philox word w whose uniform may lift bound
+// h to `floor`: the integer form of may_reach's test (U(w) = ((w >> 9) + 0.5)
+// 2^-23 >= umin iff w >> 9 >= ceil(umin 2^23 - 0.5), exact in fp32).  A group's
+// ids share the threshold of its largest bound, so a test of each word against
+// it keeps every id may_reach keeps; it is independent of the Philox chain, and
+// the words that pass it meet may_reach itself before the exact score.
+__device__ __forceinline__ uint32_t reach_word(float h, float floor) {
+  const float need = floor - h - kPruneSlack;
+  const float umin = __expf(-__expf(-need)) * (1.0f - 3e-5f);
+  const float t = ceilf(umin * 8388608.0f - 0.5f);
+  return t <= 0.f ? 0u : (t >= 8388608.f ? 0x800000u : (uint32_t)t);
+}
+
 // Four consecutive logits: 8 bytes of bf16 or 16 bytes of fp32.
 template <typename T>
 struct Raw4 {
@@ -1493,18 +1510,23 @@ __device__ __forceinline__ void score_tile(const Draw& D, int v0, int v1, const 
     Raw4<T> gd;
     if (D.R.resid) gd = lds_raw4<T>(sd + o);
     unsigned pass = 0;
+    float hmax = -CUDART_INF_F;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const float x = raw_at<T>(gt, e);
       float h;
-      if (e < ne && x >= xthr && bound_of(D, x, D.R.resid ? raw_at<T>(gd, e) : 0.f, h)) pass |= 1u << e;
+      if (e < ne && x >= xthr && bound_of(D, x, D.R.resid ? raw_at<T>(gd, e) : 0.f, h)) {
+        pass |= 1u << e;
+        hmax = fmaxf(hmax, h);
+      }
     }
     if (!pass) continue;
+    const uint32_t wmin = reach_word(hmax, floor);
     const uint4 w = gumbel_words(D.key, D.gb, D.j, (uint32_t)(v >> 2));
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      if (!((pass >> e) & 1u)) continue;
+      if (!((pass >> e) & 1u) || (ws[e] >> 9) < wmin) continue;
       const float x = raw_at<T>(gt, e);
       const float xdv = D.R.resid ? raw_at<T>(gd, e) : 0.f;
       float h;
@@ -1636,7 +1658,12 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const Params P) {
     const unsigned pub = __ldcg(P.ws.samp_floor + b);
     bool ok = true;
     if (bulk) {
-      ok = mbar_wait_bounded(&S.bar[s], (unsigned)(i / kStages) & 1u);
+      // warp 0 waits for the stage (sleeping between polls) while the other
+      // warps sleep at the barrier; then every warp observes the completed phase
+      const unsigned par = (unsigned)(i / kStages) & 1u;
+      if (threadIdx.x < 32) ok = !P.force_timeout && mbar_wait_sleepy(&S.bar[s], par);
+      ok = __syncthreads_and(ok);
+      if (ok && threadIdx.x >= 32) ok = mbar_try_wait(&S.bar[s], par) || mbar_wait_bounded(&S.bar[s], par);
       if (!ok) s_timeout = 1;
     } else {
       for (int o = threadIdx.x; o < v1 - v0; o += kThreads) {
@@ -1896,8 +1923,13 @@ static int resident_ctas(const void* fn, size_t smem = 0, int threads = kThreads
   return ctas;
 }
 
+// Test hook: when set, every bulk-copy stage wait of the next launches gives up
+// at once, as if its copy had not landed within the limit.
+static std::atomic<int> g_force_timeout{0};
+
 template <typename T, int kMode>
 static int launch(Params& P, cudaStream_t stream, const spec_verify_aux* aux) {
+  P.force_timeout = g_force_timeout.load(std::memory_order_relaxed);
   auto rec = [&](int i) {
     return (aux && aux->events[i]) ? cudaEventRecord(static_cast<cudaEvent_t>(aux->events[i]), stream)
                                    : cudaSuccess;
@@ -2180,7 +2212,9 @@ const char* spec_strerror(int status) {
   }
 }
 
-int spec_abi_version(void) { return (1 << 16) | 2; }
+int spec_abi_version(void) { return (1 << 16) | 3; }
+
+int spec_test_force_stage_timeouts(int on) { return g_force_timeout.exchange(on ? 1 : 0); }
 
 }  // extern "C"
 

@@ -33,7 +33,8 @@ def lib():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for want in ("spec_verify", "spec_verify_ex", "spec_verify_tree", "spec_verify_guided", "spec_workspace_size",
-                 "spec_workspace_init", "spec_random", "spec_strerror", "spec_abi_version", "spec_verify_noalloc"):
+                 "spec_workspace_init", "spec_random", "spec_strerror", "spec_abi_version", "spec_verify_noalloc",
+                 "spec_test_force_stage_timeouts"):
         assert want in names, names
 
 
@@ -98,7 +99,7 @@ class _Aux(ctypes.Structure):
 
 
 def test_abi_version_and_aux_layout(lib):
-    assert lib.spec_abi_version() == (1 << 16) | 2
+    assert lib.spec_abi_version() == (1 << 16) | 3
     # the 1.1 fields follow the 1.0 ones; the binding mirrors this layout
     assert _Aux.lenience.offset == _Aux.sequence_offset.offset + 4
     from speculative_decoding_draft_online_gb300 import _lib
