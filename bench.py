@@ -150,57 +150,133 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
-def cpu_oracle_run(w, seconds: float = 12.0, max_reps: int = 50):
-    """Time the oracle on a bounded sample: the first 8 sequences of the workload,
-    repeated until about `seconds` of CPU work.  Returns rows/s and a description."""
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.machine()
+
+
+def _oracle_task(task):
+    """One process of the oracle pool: verify sequences [lo, hi) of the stored workload."""
+    paths, dtype, temperature, seed, lo, hi = task
     from oracle import verify as ov
+    t, d, x = (np.load(q, mmap_mode="r") for q in paths)
+    ov.verify_stochastic(np.asarray(t[lo:hi]), np.asarray(d[lo:hi]), np.asarray(x[lo:hi]), dtype, temperature, seed,
+                         seq_offset=lo)
+    return hi - lo
+
+
+class OraclePool:
+    """The oracle over sequences on all host cores: processes started with spawn
+    (never forked from a process that holds a CUDA context), each reading the
+    workload from .npy files it maps from a temporary folder."""
+
+    def __init__(self, w):
+        import multiprocessing
+        self.w = w
+        self.dir = tempfile.mkdtemp(prefix="oracle_")
+        self.paths = []
+        for name, a in (("t", w.target), ("d", w.draft), ("x", w.tokens)):
+            q = os.path.join(self.dir, name + ".npy")
+            np.save(q, a)
+            self.paths.append(q)
+        self.cores = os.cpu_count() or 1
+        os.environ.setdefault("OMP_NUM_THREADS", "1")
+        self.pool = multiprocessing.get_context("spawn").Pool(self.cores)
+        self.pool.map(_oracle_task, [self.task(0, 1)] * self.cores)      # imports done in every process
+
+    def task(self, lo, hi):
+        return (self.paths, self.w.dtype, self.w.temperature, self.w.seed, lo, hi)
+
+    def one_pass(self) -> int:
+        """Every sequence of the workload once, one sequence per task; returns the sequences done."""
+        return sum(self.pool.map(_oracle_task, [self.task(b, b + 1) for b in range(self.w.B)], chunksize=1))
+
+    def close(self):
+        import shutil
+        self.pool.close()
+        self.pool.join()
+        shutil.rmtree(self.dir, ignore_errors=True)
+
+
+def cpu_oracle_run(w, seconds: float = 10.0):
+    """Time the oracle on the host: all cores on whole passes over the workload's
+    sequences (at least one, and up to about `seconds`), and one core on its
+    first 8 sequences (about `seconds` / 2).  Returns the cpu_baseline object."""
+    from oracle import verify as ov
+    pool = OraclePool(w)
+    try:
+        seqs, t0 = 0, time.perf_counter()
+        while True:
+            seqs += pool.one_pass()
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                break
+    finally:
+        pool.close()
+    multi = seqs * (w.k + 1) / el
     nb = 8
-    t = w.target[:nb]
-    d = w.draft[:nb]
-    x = w.tokens[:nb]
-    reps, t0 = 0, time.perf_counter()
+    reps, t1 = 0, time.perf_counter()
     while True:
-        ov.verify_stochastic(t, d, x, w.dtype, w.temperature, w.seed)
+        ov.verify_stochastic(w.target[:nb], w.draft[:nb], w.tokens[:nb], w.dtype, w.temperature, w.seed)
         reps += 1
-        el = time.perf_counter() - t0
-        if el >= seconds or reps >= max_reps:
+        el1 = time.perf_counter() - t1
+        if el1 >= seconds / 2:
             break
-    rows = reps * nb * (w.k + 1)
-    return rows / el, f"{reps} x oracle verify of sequences 0..{nb - 1} of the workload ({el:.1f} s, fp64 numpy)"
+    single = reps * nb * (w.k + 1) / el1
+    return {"value": multi, "unit": "rows/s", "cores": pool.cores, "kind": "oracle",
+            "sample": f"{seqs // w.B} passes over the workload's {w.B} sequences on {pool.cores} processes "
+                      f"({el:.1f} s, fp64 numpy)",
+            "single_core": {"value": single, "unit": "rows/s", "cores": 1,
+                            "sample": f"{reps} x sequences 0..{nb - 1} in one process ({el1:.1f} s)"},
+            "nproc": os.cpu_count(), "cpu_model": cpu_model()}
 
 
 def run_reference(args):
-    """The CPU oracle as it stands, on the machine's host cores.  A step verifies one
-    sequence of the workload (the bounded sample); the number of timed steps is
-    capped so the whole run ends within about two minutes."""
+    """The CPU oracle as it stands, on the machine's host cores: each step verifies
+    every sequence of the workload once, spread over all cores; the number of
+    timed steps is capped so the whole run ends within about two minutes."""
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    from oracle import verify as ov
     w = make_inputs()
-
-    def one(i):
-        b = i % B
-        ov.verify_stochastic(w.target[b:b + 1], w.draft[b:b + 1], w.tokens[b:b + 1], w.dtype, w.temperature, w.seed)
-
-    for i in range(min(args.warmup, 3)):
-        one(i)
-    t0 = time.perf_counter()
-    one(0)
-    per = time.perf_counter() - t0
-    steps = max(1, min(args.steps, int(120.0 / max(per, 1e-3))))
-    t_all = time.perf_counter()
-    for i in range(steps):
-        one(i)
-    el = time.perf_counter() - t_all
-    value = steps * (K + 1) / el
-    sample = f"one sequence of the workload per step ({steps} of {args.steps} requested steps timed), fp64 numpy"
+    pool = OraclePool(w)
+    try:
+        for _ in range(min(args.warmup, 1)):
+            pool.one_pass()
+        t0 = time.perf_counter()
+        pool.one_pass()
+        per = time.perf_counter() - t0
+        steps = max(1, min(args.steps, int(90.0 / max(per, 1e-3))))
+        t_all = time.perf_counter()
+        for _ in range(steps):
+            pool.one_pass()
+        el = time.perf_counter() - t_all
+    finally:
+        pool.close()
+    value = steps * B * (K + 1) / el
+    sample = (f"every sequence of the workload per step on {pool.cores} processes "
+              f"({steps} of {args.steps} requested steps timed), fp64 numpy")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": args.gpus,
         "steps": steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD, "B": B, "k": K, "V": V, "temperature": T, "input_dtype": "bf16"},
-        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": pool.cores, "kind": "oracle", "sample": sample,
+                         "nproc": os.cpu_count(), "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -330,8 +406,12 @@ def run_ours(args):
     traffic = captured_traffic()
 
     line = None
+    configs, probe = None, None
+    if rank == 0 and world == 1 and not args.no_per_config:
+        configs = per_config(dev, peaks()[0])
+        probe = read_probe(dev)
     if rank == 0:
-        cpu_rate, cpu_sample = cpu_oracle_run(w) if world == 1 and not args.no_cpu_baseline else (None, None)
+        cpu = cpu_oracle_run(w) if world == 1 and not args.no_cpu_baseline else None
         line = {
             "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / args.steps, "higher_is_better": True,
@@ -351,9 +431,12 @@ def run_ours(args):
             "gpu_launches": 2 * args.steps,
             "clocks": clocks,
         }
-        if cpu_rate is not None:
-            line["cpu_baseline"] = {"value": cpu_rate, "unit": "rows/s", "cores": 1, "kind": "oracle",
-                                    "sample": cpu_sample}
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+        if configs is not None:
+            line["config"]["per_config"] = configs
+            line["roofline"]["read_probe_gbs"] = probe
+            line["roofline"]["read_probe"] = "torch max reduction over 2 GiB of bf16 (read-only), best of 5"
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.barrier()
@@ -362,6 +445,120 @@ def run_ours(args):
 
 
 L2_BYTES = 129 * 1024 * 1024
+
+
+def graph_time(step, n_copies: int, target_steps: int = 480):
+    """Seconds per step of `step(i)` (i = 0, 1, ...; the caller rotates n_copies
+    input copies by i), captured in a CUDA graph of a multiple of n_copies steps
+    and replayed until about target_steps steps; the library launches on the
+    capturing stream.  Returns (seconds per step, steps timed)."""
+    import torch
+    for i in range(max(3, n_copies)):                  # warm, and the workspace prepared for these sizes
+        step(i)
+    torch.cuda.synchronize()
+    per_graph = n_copies * max(1, 48 // n_copies)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(per_graph):
+            step(i)
+    graph.replay()
+    torch.cuda.synchronize()
+    replays = max(1, target_steps // per_graph)
+    stream = torch.cuda.current_stream()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(replays):
+        graph.replay()
+    stop.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(stop) / 1e3 / (replays * per_graph), replays * per_graph
+
+
+def per_config(dev, peak: float):
+    """Device throughput of the five configurations: C1 tiny (fp32, stochastic and
+    greedy), C2 (stochastic), C3 greedy (the headline tensors), C4 phrase drafts
+    (a = 0.8, greedy) and C5 trees.  Each is a CUDA graph of consecutive calls
+    over enough device copies of its inputs (target and draft alike) that every
+    call reads its logits from HBM (more than twice the 129 MB L2 in total).
+    `gbs` counts each call's algorithmic bytes: B*2k*V*s of row statistics plus
+    the rows the draws read (2V*s per rejection, V*s per bonus, from the
+    outputs) in stochastic mode, B*(k+1)*V*s greedy, B*(N+1)*V*s for trees."""
+    import torch
+    import speculative_decoding_draft_online_gb300 as sv
+    import workloads as wl
+
+    def dev_rows(a, dtype):
+        a = np.ascontiguousarray(a)
+        if dtype == "bf16":
+            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(a).to(dev)
+
+    def measure(name, w, mode):
+        elem = 2 if w.dtype == "bf16" else 4
+        per_copy = w.target.nbytes + (w.draft.nbytes if mode == "stochastic" else 0)
+        n_copies = max(2, -(-2 * L2_BYTES // per_copy) + 1)
+        tgt = [dev_rows(w.target, w.dtype) for _ in range(n_copies)]
+        drf = [dev_rows(w.draft, w.dtype) for _ in range(n_copies)] if mode == "stochastic" else None
+        tokens = torch.from_numpy(np.ascontiguousarray(w.tokens)).to(dev)
+        code = sv.SPEC_BF16 if w.dtype == "bf16" else sv.SPEC_FP32
+        ws = sv.workspace(w.B, w.k, w.V, code, dev)
+        parents = torch.from_numpy(w.parents).to(dev) if mode == "tree" else None
+        out = torch.empty((w.B, w.k + 1), dtype=torch.int32, device=dev)
+        n = torch.empty((w.B,), dtype=torch.int32, device=dev)
+
+        def step(i):
+            c = i % n_copies
+            if mode == "stochastic":
+                sv.verify(tgt[c], drf[c], tokens, w.temperature, w.seed, out_tokens=out, out_n=n, ws=ws)
+            elif mode == "greedy":
+                sv.verify(tgt[c], None, tokens, 0.0, 0, out_tokens=out, out_n=n, ws=ws)
+            else:
+                sv.verify_tree(tgt[c], tokens, parents, ws=ws)
+
+        sec, steps = graph_time(step, n_copies)
+        rows = w.B * (w.k + 1)
+        if mode == "stochastic":
+            sv.verify(tgt[0], drf[0], tokens, w.temperature, w.seed, out_tokens=out, out_n=n, ws=ws)
+            torch.cuda.synchronize()
+            nh = n.cpu().numpy()
+            nbytes = w.B * 2 * w.k * w.V * elem + int(sum(2 * w.V * elem if x < w.k else w.V * elem for x in nh))
+        else:
+            nbytes = rows * w.V * elem
+        gbs = nbytes / sec / 1e9
+        del tgt, drf
+        torch.cuda.empty_cache()
+        return {"workload": name, "B": w.B, "k_or_N": w.k, "V": w.V, "dtype": w.dtype, "mode": mode,
+                "us_per_step": sec * 1e6, "rows_per_s": rows / sec, "bytes_per_step": nbytes, "gbs": gbs,
+                "frac_of_peak": gbs / peak, "steps": steps, "copies": n_copies}
+
+    c3 = make_inputs()
+    return [
+        measure("C1 tiny B4 k4 V32000 fp32 T=1", wl.c1_tiny(), "stochastic"),
+        measure("C1 tiny B4 k4 V32000 fp32, greedy", wl.c1_tiny(), "greedy"),
+        measure("C2 B32 k5 V32000 bf16 T=1", wl.c2(), "stochastic"),
+        measure("C3 B64 k8 V128256 bf16, greedy on the headline tensors", c3, "greedy"),
+        measure("C4 B16 k16 V64000 bf16 greedy, a=0.8", wl.c4(0.8), "greedy"),
+        measure("C5 B8 N26 V152064 bf16 greedy tree", wl.c5(), "tree"),
+    ]
+
+
+def read_probe(dev, nbytes: int = 2 << 30):
+    """A read-only ceiling for this GPU: torch's max reduction over a 2 GiB
+    buffer (bytes read / CUDA-event time, best of 5), reported beside the copy
+    peak of MEASURED_PEAKS.json."""
+    import torch
+    x = torch.empty(nbytes // 2, dtype=torch.bfloat16, device=dev).uniform_()
+    best = 0.0
+    for _ in range(6):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        x.max()
+        b.record()
+        torch.cuda.synchronize()
+        best = max(best, nbytes / (a.elapsed_time(b) / 1e3) / 1e9)
+    del x
+    torch.cuda.empty_cache()
+    return best
 VARIANTS = ("c3_greedy", "c3_greedy_match", "c3_lenient", "c3_top_p", "c3_top_k_top_p", "c4_guided", "c5_tree")
 
 
@@ -474,6 +671,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle CPU baseline leg")
+    ap.add_argument("--no-per-config", action="store_true", help="skip the per-configuration lines")
     ap.add_argument("--workload", choices=("c3",) + VARIANTS, default="c3",
                     help="c3 is the headline; the others print a supplementary line (one GPU)")
     args = ap.parse_args()

@@ -40,15 +40,12 @@
  *
  * Workspace: a caller-owned device buffer of spec_workspace_size() bytes.  It
  * must be zero-filled once before its first use (spec_workspace_init or any
- * memset).  A call returns the completion counters inside it to zero.  Where
- * they sit depends on (B, k or N, V), so the library clears their region first
- * (one cudaMemsetAsync of a few KB on the call's stream) when a workspace is
- * used with sizes other than those of the previous eager call on it.  A call
- * queued under stream capture always records that clear into the graph, so
- * every replay starts from zeroed counters, and once a workspace has been used
- * under capture every later eager call on it clears too (the library cannot
- * tell when the graph's replays run).  Two calls that may overlap in time must
- * not share a workspace.
+ * memset).  Every call that completes leaves all of it zeroed again (its
+ * counters, and each record once its last reader has read it), so one
+ * workspace serves calls of any sizes and modes in any order -- eager calls
+ * and replays of captured graphs alike -- with no clearing in between and no
+ * state kept on the host.  Two calls that may overlap in time must not share
+ * a workspace.  After a call that returned SPEC_ERR_CUDA, zero-fill it again.
  *
  * Errors: argument errors are detected on the host and returned before any
  * launch (nothing is written).  Conditions only visible in the data -- a NaN
@@ -234,13 +231,11 @@ int spec_random(uint64_t seed, int b, int j, int V, float* gumbel_u, float* gumb
  *   launch; use spec_verify with a workspace for those.
  *   The first call on each device looks up the array's device address (once,
  *   with that device current); make that first call before any stream capture.
- *   All calls share the one array per device and it keeps the previous call's
- *   contents (the library clears what must start at zero, as for a workspace:
- *   a call captured into a graph clears the counters on every replay, and
- *   after any capture every eager call clears them too), so calls whose work
- *   may overlap on the GPU -- other streams, other host threads, a graph
- *   replay next to an eager call -- race with each other: order them on one
- *   stream.
+ *   All calls share the one array per device.  It starts zeroed and, as a
+ *   workspace, every call leaves it zeroed, so calls of any sizes, eager or
+ *   replayed from a graph, can follow one another; but calls whose work may
+ *   overlap on the GPU -- other streams, other host threads, a graph replay
+ *   next to an eager call -- race with each other: order them on one stream.
  */
 #define SPEC_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
 int spec_verify_noalloc(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,

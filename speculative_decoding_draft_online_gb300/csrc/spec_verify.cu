@@ -49,8 +49,6 @@
 #include <cstring>
 #include <mutex>
 #include <type_traits>
-#include <unordered_map>
-#include <unordered_set>
 
 #include "spec_device.cuh"
 #include "spec_verify.h"
@@ -515,6 +513,8 @@ __device__ void greedy_match(const Params& P, int b) {
     if (P.n_committed) P.n_committed[b] = st == SPEC_OK ? committed : -1;
     if (P.status) P.status[b] = st;
   }
+  __syncwarp();
+  for (int i = lane; i <= k; i += 32) stcg_stat(P.ws.row_stat + rbase + i, RowStat{0.f, 0.f, 0, 0});
 }
 
 // Greedy tree verification.  Node m is accepted iff its parent is (the context
@@ -573,6 +573,8 @@ __device__ void tree_walk(const Params& P, int b) {
     if (P.out_leaf) P.out_leaf[b] = st == SPEC_OK ? best : -1;
     if (P.status) P.status[b] = st;
   }
+  __syncwarp();
+  for (int r = lane; r <= N; r += 32) stcg_stat(P.ws.row_stat + rbase + r, RowStat{0.f, 0.f, 0, 0});
 }
 
 // A row's last piece has landed: merge its partials into the row statistics
@@ -581,16 +583,18 @@ template <typename T, int kMode>
 __device__ void finish_row(const Params& P, long long r, int b) {
   const int lane = threadIdx.x & 31;
   __threadfence();
-  const float4* src = reinterpret_cast<const float4*>(P.ws.row_partial + r * P.nt);
-  float m = -CUDART_INF_F, s = 0.f;
-  int ix = INT_MAX, bad = 0, tmo = 0;
+  float4* src = reinterpret_cast<float4*>(P.ws.row_partial + r * P.nt);
+  float m = -CUDART_INF_F, s = 0.f, fm = -CUDART_INF_F;
+  int ix = INT_MAX, ft = INT_MAX, bad = 0, tmo = 0;
   for (int t = lane; t < P.nt; t += 32) {
     const float4 p = __ldcg(src + t);
+    __stcg(src + t, make_float4(0.f, 0.f, 0.f, 0.f));  // read for the last time: the workspace is left zeroed
     if (p.w != 0.f) { tmo = 1; continue; }          // a piece whose data never arrived
     if (p.x != p.x) { bad = 1; continue; }
     if constexpr (kMode == kStochastic) {
       const float M = fmaxf(m, p.x);
       s = rescale(s, m, M, P.c) + rescale(p.y, p.x, M, P.c);
+      if (p.x > fm) { fm = p.x; ft = t; }           // the piece holding the max starts at tile ft
     } else {
       const int pi = __float_as_int(p.z);
       if (beats(p.x, pi, m, ix)) ix = pi;
@@ -603,8 +607,11 @@ __device__ void finish_row(const Params& P, long long r, int b) {
     s = warp_sum(rescale(s, m, M, P.c));
     bad = __any_sync(0xffffffffu, bad);
     tmo = __any_sync(0xffffffffu, tmo);
+    warp_argmax(fm, ft);
     const bool finite = M > -CUDART_INF_F && M < CUDART_INF_F && s > 0.f && s < CUDART_INF_F;
-    st = RowStat{M, logf(s), INT_MAX, tmo ? SPEC_ERR_TIMEOUT : (bad || !finite) ? SPEC_ERR_NONFINITE : SPEC_OK};
+    // stochastic rows keep, in place of an argmax, the first tile of the piece
+    // holding the row's max: where a draw from the row starts
+    st = RowStat{M, logf(s), ft, tmo ? SPEC_ERR_TIMEOUT : (bad || !finite) ? SPEC_ERR_NONFINITE : SPEC_OK};
   } else {
     warp_argmax(m, ix);
     bad = __any_sync(0xffffffffu, bad);
@@ -1635,15 +1642,7 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const Params P) {
     D.R.mt = rt.m;
     D.R.lnSt = lnSt;
     D.R.cdelta = -(rd.m - rt.m) * P.invT - (lnSd - lnSt);
-    const Partial* piece = P.ws.row_partial + rt_i * P.nt;
-    float bm = -CUDART_INF_F;
-    int bi = INT_MAX;
-    for (int t = threadIdx.x; t < P.nt; t += kThreads) {
-      const float pm = __ldcg(&piece[t].m);
-      if (pm > bm) { bm = pm; bi = t; }
-    }
-    block_argmax(bm, bi, sh);
-    ft = bi < P.nt ? bi : 0;
+    ft = rt.arg >= 0 && rt.arg < P.nt ? rt.arg : 0;   // the first tile of the piece holding the row's max
     if (bulk && threadIdx.x == 0) issue(0);
   }
   uint32_t* queue = S.queue[threadIdx.x >> 5];
@@ -1752,6 +1751,7 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const Params P) {
   int timed_out = 0;
   for (int q = threadIdx.x; q < P.ns; q += kThreads) {
     const float2 p = __ldcg(P.ws.samp_partial + (size_t)b * P.ns + q);
+    __stcg(P.ws.samp_partial + (size_t)b * P.ns + q, make_float2(0.f, 0.f));   // the workspace is left zeroed
     const int pi = __float_as_int(p.y);
     if (pi == -2) { timed_out = 1; continue; }
     if (p.x != p.x) { bad = 1; continue; }
@@ -1778,6 +1778,16 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const Params P) {
       }
     }
     block_argmax(best, bidx, sh);
+  }
+  // every CTA of the sequence has read its statistics and state: the
+  // workspace is left zeroed
+  {
+    const long long rb = (long long)b * P.rows_per_seq;
+    for (int r = threadIdx.x; r < P.rows_per_seq; r += kThreads) {
+      stcg_stat(P.ws.row_stat + rb + r, RowStat{0.f, 0.f, 0, 0});
+      if (P.filtering) __stcg(P.ws.row_filter + rb + r, make_float2(0.f, 0.f));
+    }
+    if (threadIdx.x == 0) __stcg(reinterpret_cast<int2*>(P.ws.seq) + b, make_int2(0, 0));
   }
   if (threadIdx.x >= 32) return;
   int32_t* out = P.out_tokens + (size_t)b * P.out_w;
@@ -1809,9 +1819,8 @@ __global__ void random_kernel(uint2 key, int b, int j, int V, float* gu, float* 
 
 // --------------------------------------------------------------- host side ---
 
-// The workspace: first the counters that must read zero when a call starts
-// (one contiguous region, so clearing them is one small memset), then the
-// records every call writes before it reads them.
+// The workspace: the completion counters, then the records every call writes
+// before it reads them.  A call leaves all of it zeroed (see below).
 struct Layout {
   size_t row_cnt, seq_cnt, samp_cnt, samp_floor, counters_end;   // the zeroed region [0, counters_end)
   size_t row_partial, row_stat, row_filter, seq, samp_partial, total;
@@ -1858,48 +1867,13 @@ static Workspace bind(void* base, const Layout& L) {
 
 static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Every call returns the counters it used to zero, but where they sit depends
-// on the sizes, so a workspace that served other sizes holds other records
-// there.  The counter region is then cleared first (one cudaMemsetAsync on the
-// call's stream).  The library remembers, per workspace, the sizes of the last
-// call queued eagerly on it and skips the clear when they repeat.  That record
-// follows the host's queueing order, not the GPU's execution order, which a
-// captured graph breaks (its replays run whenever the caller launches them):
-// so a call queued under stream capture always records the clear into the
-// graph (each replay clears), and a workspace once used under capture is
-// cleared by every later eager call too.
-struct Sizes {
-  int B, k, V;
-  bool operator==(const Sizes& o) const { return B == o.B && k == o.k && V == o.V; }
-};
-
-static int prepare_workspace(void* ws, const Layout& L, int B, int k, int V, cudaStream_t stream) {
-  static std::mutex mu;
-  static std::unordered_map<uintptr_t, Sizes> last;       // eager calls on never-captured workspaces
-  static std::unordered_set<uintptr_t> captured;          // workspaces used under stream capture
-  const uintptr_t key = reinterpret_cast<uintptr_t>(ws);
-  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-  const bool known = cudaStreamIsCapturing(stream, &cs) == cudaSuccess;
-  bool clear = true;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (!known || cs != cudaStreamCaptureStatusNone) {
-      captured.insert(key);
-      last.erase(key);
-    } else if (!captured.count(key)) {
-      auto it = last.find(key);
-      clear = !(it != last.end() && it->second == Sizes{B, k, V});
-      last[key] = Sizes{B, k, V};
-    }
-  }
-  if (!known) (void)cudaGetLastError();
-  if (clear && cudaMemsetAsync(ws, 0, L.counters_end, stream) != cudaSuccess) {
-    std::lock_guard<std::mutex> lock(mu);
-    last.erase(key);
-    return SPEC_ERR_CUDA;
-  }
-  return SPEC_OK;
-}
+// The workspace between calls.  Every call leaves zeroed everything it wrote
+// there: its counters, and each record once its last reader has read it (a
+// row's partials when the row is merged, the rows' statistics and filters,
+// the sequence state and the draw partials when the sequence's output is
+// written).  So whatever sizes the calls use, and whether they run eagerly or
+// as replays of a captured graph, a call finds the workspace all zero -- as
+// it was first handed over -- and needs no clearing.
 
 // Resident CTAs of a kernel with `threads` threads and `smem` bytes of dynamic
 // shared memory on the current device, cached per (device, kernel).
@@ -2084,7 +2058,6 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, const in
     P.tail_runs = aux->tail_runs;
   }
   cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
-  if ((rc = prepare_workspace(workspace, L, B, k, V, stream)) != SPEC_OK) return rc;
   if (greedy) {
     P.rows_per_seq = k + 1;
     P.R = (long long)B * (k + 1);
@@ -2144,7 +2117,6 @@ int spec_verify_tree(const void* target_logits, const int32_t* node_tokens, cons
   P.status = status;
   P.ws = bind(workspace, L);
   cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
-  if ((rc = prepare_workspace(workspace, L, B, N, V, stream)) != SPEC_OK) return rc;
   return dtype == SPEC_BF16 ? launch<uint16_t, kTree>(P, stream, nullptr) : launch<float, kTree>(P, stream, nullptr);
 }
 
@@ -2184,7 +2156,6 @@ int spec_verify_guided(const void* target_logits, const int32_t* draft_tokens, c
   P.rows_per_seq = k + 1;
   P.R = (long long)B * (k + 1);
   cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
-  if ((rc = prepare_workspace(workspace, Lw, B, k, V, stream)) != SPEC_OK) return rc;
   return dtype == SPEC_BF16 ? launch<uint16_t, kGreedy>(P, stream, nullptr) : launch<float, kGreedy>(P, stream, nullptr);
 }
 
@@ -2261,12 +2232,8 @@ extern "C" int spec_verify_noalloc(const void* target_logits, const void* draft_
   void* scratch = nullptr;
   const int rc = sv::noalloc_scratch_address(&scratch);
   if (rc != SPEC_OK) return rc;
-  // The scratch keeps whatever the previous call left in it.  The counters
-  // that must start at zero are returned to zero by every call.  spec_verify_ex
-  // clears their region first when the sizes differ from those of the previous
-  // eager call on this scratch, on every call queued under stream capture (the
-  // clear becomes part of the graph), and on every call once the scratch has
-  // been used under capture.
+  // The scratch starts zeroed (a static device array) and every call leaves
+  // it zeroed, whatever its sizes: no call needs to clear it.
   return spec_verify_ex(target_logits, draft_logits, draft_tokens, B, k, V, dtype, temperature, seed, out_tokens,
                         out_n_accepted, scratch, sv::kNoAllocScratchBytes, cuda_stream, nullptr);
 }

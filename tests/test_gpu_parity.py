@@ -273,6 +273,48 @@ def test_workspace_reuse_across_graph_capture(sv):
         assert torch.equal(out[0], g_ref[0]) and torch.equal(out[1], g_ref[1]), step
 
 
+def test_workspace_is_left_zeroed(sv):
+    """Every call leaves the whole workspace zeroed, whatever its mode and sizes:
+    stochastic with and without top-p, greedy with the match outputs, guided,
+    tree, and calls whose bulk-copy waits time out."""
+    ws = sv.workspace(64, 16, 200000, sv.SPEC_BF16, "cuda")
+    a = wl.gaussian_pair(6, 5, 3333, wl.BF16, 0.8, seed=3, sigma_t=3.0, sigma_d=1.0)
+    c2 = wl.c2(seed=8)
+    g = wl.c4(0.7, seed=4, B=5, k=9, V=4000)
+    tr = wl.c5(B=2, V=5000)
+    guided_w, guide = wl.guided_drafts(0.8, 0.9, 12, seed=5, B=4, k=8, V=3000)
+    dev = lambda w: (to_device(w.target, w.dtype), None if w.draft is None else to_device(w.draft, w.dtype),
+                     tokens_to_device(w.tokens))
+
+    def zero():
+        torch.cuda.synchronize()
+        return int(torch.count_nonzero(ws).item()) == 0
+
+    t, d, x = dev(a)
+    sv.verify_ex(t, d, x, 0.8, 7, ws=ws, aux=True)
+    assert zero()
+    t, d, x = dev(c2)
+    sv.verify_ex(t, d, x, 1.0, 9, ws=ws, top_p=0.8, top_k=40)
+    assert zero()
+    t, _, x = dev(g)
+    sv.verify_ex(t, None, x, 0.0, 0, ws=ws, match=True, committed=True)
+    assert zero()
+    t, _, x = dev(guided_w)
+    sv.verify_guided(t, x, tokens_to_device(guide), ws=ws)
+    assert zero()
+    t, _, x = dev(tr)
+    sv.verify_tree(t, x, tokens_to_device(tr.parents), ws=ws)
+    assert zero()
+    prev = sv.force_stage_timeouts(True)
+    try:
+        t, d, x = dev(c2)
+        _, n = sv.verify(t, d, x, 1.0, 9, ws=ws)
+        torch.cuda.synchronize()
+    finally:
+        sv.force_stage_timeouts(prev)
+    assert torch.all(n == -1) and zero()
+
+
 def test_side_stream(sv):
     w = wl.gaussian_pair(4, 4, 5000, wl.BF16, 1.0, seed=21, sigma_t=3.0, sigma_d=1.0)
     s = torch.cuda.Stream()
@@ -282,6 +324,64 @@ def test_side_stream(sv):
     s.synchronize()
     ref = ov.verify_stochastic(w.target, w.draft, w.tokens, w.dtype, 1.0, 5)
     TALLY.add(compare_stochastic(ref, out.cpu().numpy(), n.cpu().numpy(), np.zeros(4, np.int32), w.k))
+
+
+def _unclipped_rows(seed, shape, V):
+    """N(0, 4^2) rows rounded to bf16, unclipped: near the top of a row the bf16
+    grid is 1/8 wide, so some rows hold their maximum at two or more ids."""
+    rng = np.random.default_rng(seed)
+    t = wl.store(rng.standard_normal(shape + (V,), dtype=np.float32) * np.float32(4.0), wl.BF16)
+    dec = ov.decode_logits(t, "bf16")
+    mx = dec.max(-1)
+    ties = (dec == mx[..., None]).sum(-1)
+    # the highest index holding each row's max (a wrong tie-break would pick it)
+    last = (dec.shape[-1] - 1) - np.argmax(dec[..., ::-1] == mx[..., None], axis=-1)
+    return rng, t, ties, last.astype(np.int32)
+
+
+def test_c4_full_size_with_ties(sv):
+    """C4's shape (B16 k16 V64000 bf16, a = 0.8) on unclipped rows: the target
+    argmax is whatever the oracle finds, lowest index among ties, and a draft at
+    a tied row sometimes names the highest tied index instead."""
+    B, k, V = 16, 16, 64000
+    rng, t, ties, last = _unclipped_rows(404, (B, k + 1), V)
+    assert (ties > 1).sum() >= 5                       # rows with a tie at the max do occur
+    a = ov.row_argmax(ov.decode_logits(t, "bf16"))
+    other = ((a[:, :k] + 1 + rng.integers(0, V - 1, size=(B, k))) % V).astype(np.int32)
+    tokens = np.where(rng.random((B, k)) < 0.8, a[:, :k], other).astype(np.int32)
+    tied = ties[:, :k] > 1
+    tokens = np.where(tied & (rng.random((B, k)) < 0.5), last[:, :k], tokens).astype(np.int32)
+    out, n = sv.verify(to_device(t, "bf16"), None, tokens_to_device(tokens), 0.0)
+    torch.cuda.synchronize()
+    ref = ov.verify_greedy(t, tokens, "bf16")
+    np.testing.assert_array_equal(out.cpu().numpy(), ref.out_tokens)
+    np.testing.assert_array_equal(n.cpu().numpy(), ref.n_accepted)
+    assert np.any(tied & (tokens == last[:, :k]) & (tokens != a[:, :k]))   # a tie's later index was drafted
+
+
+def test_c5_full_size_with_ties(sv):
+    """C5's shape (B8, 26-node trees, V152064 bf16) on unclipped rows: a node's
+    token is its parent row's argmax (lowest index among ties) w.p. 0.7, and at
+    a tied parent row sometimes the highest tied index instead."""
+    par = wl.tree_shape()
+    B, N, V = 8, par.shape[0], 152064
+    rng, t, ties, last = _unclipped_rows(405, (B, N + 1), V)
+    assert (ties > 1).sum() >= 5
+    a = ov.row_argmax(ov.decode_logits(t, "bf16"))
+    prow = np.where(par < 0, 0, par + 1)
+    want = a[:, prow]
+    other = ((want + 1 + rng.integers(0, V - 1, size=(B, N))) % V).astype(np.int32)
+    tokens = np.where(rng.random((B, N)) < 0.7, want, other)
+    tied = ties[:, prow] > 1
+    tokens = np.where(tied & (rng.random((B, N)) < 0.5), last[:, prow], tokens).astype(np.int32)
+    parents = np.broadcast_to(par, (B, N)).copy()
+    out, n, leaf, status = sv.verify_tree(to_device(t, "bf16"), tokens_to_device(tokens), tokens_to_device(parents))
+    torch.cuda.synchronize()
+    ref = ov.verify_tree(t, tokens, parents, "bf16")
+    np.testing.assert_array_equal(status.cpu().numpy(), ref.status)
+    np.testing.assert_array_equal(out.cpu().numpy(), ref.out_tokens)
+    np.testing.assert_array_equal(n.cpu().numpy(), ref.n_accepted)
+    np.testing.assert_array_equal(leaf.cpu().numpy(), ref.leaf)
 
 
 @pytest.mark.parametrize("shape", ["chain", "wide", "random"])
