@@ -436,7 +436,8 @@ def run_ours(args):
         if configs is not None:
             line["config"]["per_config"] = configs
             line["roofline"]["read_probe_gbs"] = probe
-            line["roofline"]["read_probe"] = "torch max reduction over 2 GiB of bf16 (read-only), best of 5"
+            line["roofline"]["read_probe"] = ("spec_probe_read: the row pass's loads alone (persistent grid, "
+                                              "16-byte no-L1 loads, 4 per thread in flight) over 2 GiB, best of 5")
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.barrier()
@@ -543,22 +544,25 @@ def per_config(dev, peak: float):
 
 
 def read_probe(dev, nbytes: int = 2 << 30):
-    """A read-only ceiling for this GPU: torch's max reduction over a 2 GiB
-    buffer (bytes read / CUDA-event time, best of 5), reported beside the copy
-    peak of MEASURED_PEAKS.json."""
+    """The read ceiling for the row pass's load pattern: the library's read
+    probe (the row pass's loads and nothing else, as many CTAs as fit) over a
+    2 GiB buffer, bytes / CUDA-event time, best of 5."""
     import torch
+    import speculative_decoding_draft_online_gb300 as sv
     x = torch.empty(nbytes // 2, dtype=torch.bfloat16, device=dev).uniform_()
     best = 0.0
     for _ in range(6):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
-        x.max()
+        sv.probe_read(x)
         b.record()
         torch.cuda.synchronize()
         best = max(best, nbytes / (a.elapsed_time(b) / 1e3) / 1e9)
     del x
     torch.cuda.empty_cache()
     return best
+
+
 VARIANTS = ("c3_greedy", "c3_greedy_match", "c3_lenient", "c3_top_p", "c3_top_k_top_p", "c4_guided", "c5_tree")
 
 

@@ -271,6 +271,18 @@ int spec_verify_guided(const void* target_logits, const int32_t* draft_tokens, c
                        int32_t* status, void* workspace, size_t workspace_bytes, void* cuda_stream);
 
 /*
+ * spec_probe_read -- measurement helper (not on the hot path): reads `bytes`
+ * (rounded down to 16) of device memory at `data` (16-byte aligned) with the
+ * row pass's load pattern and nothing else -- a persistent grid of `ctas` CTAs
+ * (0 = as many as fit on the GPU at once) over contiguous ranges, 16-byte
+ * loads that bypass L1, four per thread in flight -- and xors the words into
+ * sink[0 .. ctas-1] (device; the caller zero-fills it).  Time it with events on
+ * `cuda_stream`: bytes / time is the read ceiling the row pass streams against.
+ * Returns SPEC_OK or SPEC_ERR_ARG / SPEC_ERR_CUDA.
+ */
+int spec_probe_read(const void* data, size_t bytes, unsigned* sink, int ctas, void* cuda_stream);
+
+/*
  * spec_test_force_stage_timeouts -- test hook (since ABI 1.3), off by default.
  *   on != 0: from the next call on, every wait of a bulk-copy stage (the ring
  *   row pass of large greedy and tree batches, and the sampling pass of

@@ -7,7 +7,7 @@ behind the C ABI declared in include/spec_verify.h.  This package is the thin
 Python binding of that library (torch supplies device memory and streams).
 """
 from ._lib import (SPEC_BF16, SPEC_ERR_NONFINITE, SPEC_ERR_TOKEN, SPEC_FP32, LIB_PATH, SpecError, lib,  # noqa: F401
-                   force_stage_timeouts, random_stream, verify, verify_ex, verify_guided, verify_tree, workspace,
+                   force_stage_timeouts, probe_read, random_stream, verify, verify_ex, verify_guided, verify_tree, workspace,
                    workspace_size)
 
 __all__ = ["verify", "verify_ex", "verify_tree", "verify_guided", "workspace", "workspace_size", "random_stream",

@@ -68,6 +68,8 @@ def _load():
     L.spec_strerror.restype = ctypes.c_char_p
     L.spec_abi_version.argtypes = []
     L.spec_abi_version.restype = i32
+    L.spec_probe_read.argtypes = [vp, sz, vp, i32, vp]
+    L.spec_probe_read.restype = i32
     L.spec_test_force_stage_timeouts.argtypes = [i32]
     L.spec_test_force_stage_timeouts.restype = i32
     if L.spec_abi_version() < ABI_MIN or (L.spec_abi_version() >> 16) != (ABI_MIN >> 16):
@@ -289,3 +291,14 @@ def force_stage_timeouts(on: bool) -> bool:
     """Test hook: make every bulk-copy stage wait of later calls give up at once
     (spec_test_force_stage_timeouts).  Returns the previous setting."""
     return bool(lib.spec_test_force_stage_timeouts(1 if on else 0))
+
+
+def probe_read(buf: torch.Tensor, ctas: int = 0, stream=None) -> None:
+    """spec_probe_read over a contiguous device tensor (measurement helper)."""
+    if not buf.is_cuda or not buf.is_contiguous():
+        raise ValueError("probe_read needs a contiguous CUDA tensor")
+    sink = torch.zeros(max(ctas, 4096), dtype=torch.int32, device=buf.device)
+    rc = lib.spec_probe_read(_ptr(buf), buf.numel() * buf.element_size(), _ptr(sink), ctas,
+                             _stream_ptr(stream, buf.device))
+    if rc != SPEC_OK:
+        raise SpecError(rc, "spec_probe_read")

@@ -1817,12 +1817,37 @@ __global__ void random_kernel(uint2 key, int b, int j, int V, float* gu, float* 
   }
 }
 
+// ------------------------------------------------------------ read probe ---
+// The row pass's load pattern with nothing else: a persistent grid of
+// contiguous ranges, 16-byte no-L1 loads, kUnroll per thread in flight, the
+// words folded by xor so that no load is dead.  Its rate is the read ceiling
+// the row pass streams against.
+__global__ void __launch_bounds__(kThreads, 6) probe_read_kernel(const uint4* data, long long nvec, unsigned* sink) {
+  const long long v0 = nvec * blockIdx.x / gridDim.x, v1 = nvec * (blockIdx.x + 1) / gridDim.x;
+  constexpr int kBatch = kUnroll * kThreads;
+  unsigned acc = 0;
+  long long i = v0 + threadIdx.x;
+  for (; i + (kUnroll - 1) * kThreads < v1; i += kBatch) {
+    uint4 v[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) v[u] = ld_stream16(data + i + u * kThreads);
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) acc ^= v[u].x ^ v[u].y ^ v[u].z ^ v[u].w;
+  }
+  for (; i < v1; i += kThreads) {
+    const uint4 v = ld_stream16(data + i);
+    acc ^= v.x ^ v.y ^ v.z ^ v.w;
+  }
+  acc = __reduce_xor_sync(0xffffffffu, acc);
+  if ((threadIdx.x & 31) == 0) atomicXor(sink + blockIdx.x, acc);
+}
+
 // --------------------------------------------------------------- host side ---
 
 // The workspace: the completion counters, then the records every call writes
 // before it reads them.  A call leaves all of it zeroed (see below).
 struct Layout {
-  size_t row_cnt, seq_cnt, samp_cnt, samp_floor, counters_end;   // the zeroed region [0, counters_end)
+  size_t row_cnt, seq_cnt, samp_cnt, samp_floor, counters_end;
   size_t row_partial, row_stat, row_filter, seq, samp_partial, total;
   int nt;
   long long rmax;
@@ -2165,6 +2190,16 @@ int spec_random(uint64_t seed, int b, int j, int V, float* gumbel_u, float* gumb
   const int groups = (V + 3) / 4;
   random_kernel<<<(groups + kThreads - 1) / kThreads, kThreads, 0, static_cast<cudaStream_t>(cuda_stream)>>>(
       make_uint2((uint32_t)seed, (uint32_t)(seed >> 32)), b, j, V, gumbel_u, gumbel_g, accept_u);
+  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+int spec_probe_read(const void* data, size_t bytes, unsigned* sink, int ctas, void* cuda_stream) {
+  if (!data || !sink || bytes < 16 || !aligned(data, 16) || ctas < 0) return SPEC_ERR_ARG;
+  int grid = ctas;
+  if (grid == 0) grid = resident_ctas(reinterpret_cast<const void*>(&probe_read_kernel));
+  if (grid <= 0) return SPEC_ERR_CUDA;
+  probe_read_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(cuda_stream)>>>(
+      static_cast<const uint4*>(data), (long long)(bytes / 16), sink);
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 

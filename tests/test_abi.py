@@ -34,7 +34,7 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for want in ("spec_verify", "spec_verify_ex", "spec_verify_tree", "spec_verify_guided", "spec_workspace_size",
                  "spec_workspace_init", "spec_random", "spec_strerror", "spec_abi_version", "spec_verify_noalloc",
-                 "spec_test_force_stage_timeouts"):
+                 "spec_test_force_stage_timeouts", "spec_probe_read"):
         assert want in names, names
 
 

@@ -48,3 +48,15 @@ def test_workspace_size_rejects_invalid_sizes(sv):
     assert sv.workspace_size(4, 4, 32000) > 0
     with pytest.raises(ValueError):
         sv.workspace(0, 4, 32000, sv.SPEC_BF16, "cpu")
+
+
+def test_bench_command_line_parses():
+    """bench.py's argument parsing runs on a host without a GPU (every option the driver passes)."""
+    import subprocess
+    import sys as _sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([_sys.executable, os.path.join(root, "bench.py"), "--help"], capture_output=True, text=True,
+                         timeout=120)
+    assert out.returncode == 0, out.stderr
+    for opt in ("--gpus", "--steps", "--warmup", "--impl", "--workload", "--no-per-config"):
+        assert opt in out.stdout
