@@ -238,8 +238,8 @@ def test_workspace_reuse_and_determinism(sv):
 def test_workspace_reuse_across_graph_capture(sv):
     """One workspace serves eager calls at one size and a graph captured at
     another, interleaved on one stream; every result equals a fresh
-    workspace's (the counters are cleared wherever consecutive executions may
-    differ in size, whatever order the replays run in)."""
+    workspace's (every execution leaves the workspace zeroed, so nothing
+    depends on the order of eager calls and replays)."""
     ws = sv.workspace(64, 16, 200000, sv.SPEC_BF16, "cuda")
     a = wl.gaussian_pair(6, 5, 3333, wl.BF16, 0.8, seed=3, sigma_t=3.0, sigma_d=1.0)
     g = wl.c4(0.7, seed=4, B=5, k=9, V=4000)

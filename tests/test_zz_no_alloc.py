@@ -6,7 +6,7 @@ synchronisation is not allowed -- so they cannot hand spec_verify a workspace.
 spec_verify_noalloc keeps the kernels' scratch in a fixed array inside the
 library instead.  These tests call it through the C ABI and check that it
 returns what spec_verify returns, on consecutive calls with different sizes
-and modes (the shared scratch keeps the previous call's contents), inside and
+and modes (one shared scratch serves them all), inside and
 around captured CUDA graphs, that it agrees with the CPU oracle on its own, and
 that sizes beyond the array are refused before any launch.
 
@@ -91,8 +91,8 @@ def test_noalloc_agrees_with_the_oracle(abi):
 def test_noalloc_in_and_around_captured_graphs(abi):
     """Eager calls at one size, a graph captured at another, eager calls at the
     graph's size and replays, interleaved on one stream: every result equals
-    spec_verify's on the same inputs (the scratch's counters are cleared
-    wherever the sizes of consecutive executions may differ)."""
+    spec_verify's on the same inputs (every execution leaves the scratch
+    zeroed, whatever its sizes)."""
     sv, lib = abi
     a = wl.c2(seed=81)                                # B=32 k=5 V=32000, stochastic
     g = wl.c4(0.8, seed=82)                           # B=16 k=16 V=64000, greedy
