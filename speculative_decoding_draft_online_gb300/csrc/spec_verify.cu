@@ -44,6 +44,7 @@
 
 #include <atomic>
 #include <climits>
+#include <cstddef>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -884,7 +885,9 @@ __global__ void __launch_bounds__(kRingThreads, kRingMinCtas) row_pass_ring(cons
 // samples with top-p 0.8): every target and draft row of a sequence goes
 // through the same filter before the rule.  Order: temperature, top-k, then
 // top-p on the top-k distribution.  Both are value thresholds, so ties at a
-// threshold are kept.  One CTA per row finds each threshold in two steps:
+// threshold are kept.  One cluster of CTAs per row (each CTA scans one
+// segment of the row; their histograms are summed at the cluster's first CTA
+// through distributed shared memory) finds each threshold in two steps:
 //   1. histograms of count and mass exp((x - m) / T) by distance below the row
 //      max (m from the row pass) pick the bin where the count (top-k) or the
 //      mass (top-p) summed from the top first reaches its target.  The bins
@@ -894,10 +897,15 @@ __global__ void __launch_bounds__(kRingThreads, kRingMinCtas) row_pass_ring(cons
 //      Only the ids near the top take shared-memory atomics, spread over many
 //      bins.
 //   2. the bin holds a contiguous range of order-preserving keys of the raw
-//      logits, found by bisection; when it spans fewer than 2048 keys (always
-//      for bf16 near the top) one pass histograms key - smallest, otherwise
-//      radix rounds over the key bits (11 a round) decide the exact value.
-// Masses are summed as 64-bit fixed point (2^-40 units) with integer atomics.
+//      logits, found by a parallel search; when it spans fewer than 2048 keys
+//      (always for bf16 near the top) one pass histograms key - smallest,
+//      otherwise radix rounds over the key bits (11 a round) decide the exact
+//      value.
+// Every pass tests each 16-byte vector first, from its largest and smallest
+// logit, and only vectors that straddle a boundary take the per-id test.
+// Masses are summed as 64-bit fixed point (2^-40 units) with 32-bit integer
+// atomics, exactly and in any order.  Top-p after top-k reuses the top-k
+// pass's window-0 histogram when the top-k key was found there.
 
 constexpr int kHistBits = 11;
 constexpr int kHistBins = 1 << kHistBits;
@@ -937,54 +945,165 @@ __device__ __forceinline__ float win_start(int w) {
   return w == 0 ? 0.f : (w == 1 ? 2047.f / 170.f : 2047.f / 170.f + 2047.f / 8.f);
 }
 
-// A row's windows as affine maps of the logit: window w's scaled position of x
-// is s_w(x) = fma(-x, a_w, b_w) = ((m - x) / T - start_w) * scale_w, rounded
-// once; non-increasing in x.
-struct Windows {
-  float a[kWindows], b[kWindows];
-  __device__ Windows(float m, float invT) {
-#pragma unroll
-    for (int w = 0; w < kWindows; ++w) {
-      a[w] = invT * win_scale(w);
-      b[w] = (m * invT - win_start(w)) * win_scale(w);
-    }
+// Window w of a row as an affine map of the logit: its scaled position of x is
+// s_w(x) = fma(-x, a, b) = ((m - x) / T - start_w) * scale_w, rounded once and
+// non-increasing in x.  Window w begins where window w - 1's tail begins, so an
+// id outside window w - 1's tail lies above window w (and every earlier
+// window's tail holds window w - 1's).
+struct WinMap {
+  float ap, bp;       // window w - 1 (w > 0)
+  float a, b;         // window w
+  bool first;         // w == 0
+  __device__ WinMap(float m, float invT, int w) : first(w == 0) {
+    const int p = w > 0 ? w - 1 : 0;
+    a = invT * win_scale(w);
+    b = (m * invT - win_start(w)) * win_scale(w);
+    ap = invT * win_scale(p);
+    bp = (m * invT - win_start(p)) * win_scale(p);
   }
-  // Where x falls in window w: kDistBins if above the window (not in the tail
-  // of every earlier window), else 0 for the window's tail or its bin 1..2047.
+  __device__ __forceinline__ bool above(float x) const {
+    return !first && !(fmaf(-x, ap, bp) >= (float)(kDistBins - 1));
+  }
+  // kDistBins above the window, 0 in its tail, else its bin 1..2047.
   // Non-decreasing in x.
-  __device__ __forceinline__ int bin(float x, int w) const {
-    for (int j = 0; j < w; ++j)
-      if (!(fmaf(-x, a[j], b[j]) >= (float)(kDistBins - 1))) return kDistBins;
-    const float s = fmaxf(fmaf(-x, a[w], b[w]), 0.f);
+  __device__ __forceinline__ int bin(float x) const {
+    if (above(x)) return kDistBins;
+    const float s = fmaxf(fmaf(-x, a, b), 0.f);
     return s < (float)(kDistBins - 1) ? (kDistBins - 1) - (int)s : 0;
   }
 };
+
+// Largest and smallest logit of a 16-byte vector (the rows the filter sees
+// hold no NaN: a row with one reports an error and is not filtered).
+template <typename T>
+__device__ __forceinline__ void vec_range(const uint4& v, float& hi, float& lo) {
+  if constexpr (sizeof(T) == 2) {
+    const uint32_t mx = bf16x2_nanmax(bf16x2_nanmax(v.x, v.y), bf16x2_nanmax(v.z, v.w));
+    const uint32_t mn = bf16x2_min(bf16x2_min(v.x, v.y), bf16x2_min(v.z, v.w));
+    hi = fmaxf(bf16_lo(mx), bf16_hi(mx));
+    lo = fminf(bf16_lo(mn), bf16_hi(mn));
+  } else {
+    hi = fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)), fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
+    lo = fminf(fminf(__uint_as_float(v.x), __uint_as_float(v.y)), fminf(__uint_as_float(v.z), __uint_as_float(v.w)));
+  }
+}
+
+// The histogram passes test each 16-byte vector first (from its largest and
+// smallest logit): most vectors take no part or are counted whole.  The rest
+// go through the warp's queue, and the warp's lanes share their ids out, so
+// the per-id test runs with every lane busy.  Only scan_segment's full batches
+// come here: every thread of the CTA takes part in them, as the warp-wide
+// ballot and syncs need; its remainder loop, where a warp may be partly idle,
+// tests every id.
+template <typename T, class Acc>
+__device__ __forceinline__ void warp_queue_ids(Acc& acc, uint4* q, const uint4& v, bool slow) {
+  const int lane = threadIdx.x & 31;
+  const unsigned m = __ballot_sync(0xffffffffu, slow);
+  if (!m) return;
+  if (slow) q[__popc(m & ((1u << lane) - 1u))] = v;
+  __syncwarp();
+  const int n = __popc(m) * Vec<T>::n;
+  for (int i = lane; i < n; i += 32) acc.elem(Vec<T>::at(q[i / Vec<T>::n], i % Vec<T>::n));
+  __syncwarp();                          // the queue is refilled by the next vector
+}
 
 constexpr float kMassUnit = 1099511627776.0f;   // 2^40: fixed-point scale of a mass in (0, 1]
 
 struct FilterScratch {
   uint32_t cnt[kHistBins];
   float mass[kHistBins];
-  unsigned long long massq[kHistBins];   // fixed-point sums, turned into `mass` after a pass
+  // fixed-point sums of the masses (2^-40 units, exact and independent of the
+  // order of the adds) as 32-bit halves, turned into `mass` after a pass
+  uint32_t mlo[kHistBins], mhi[kHistBins];
   uint32_t wc[kWarps];
   float wm[kWarps];
   uint4 vq[kWarps][32];                  // per warp: 16-byte vectors that need the per-id test
+  // select_bin's result (six words, sent to the cluster's other CTAs as such)
   int sel_bin;
   uint32_t sel_cnt_above, sel_cnt_bin, total_cnt;
   float sel_mass_above, sel_mass_bin;
 };
+constexpr int kPickWords = 6;
+static_assert(offsetof(FilterScratch, sel_mass_bin) - offsetof(FilterScratch, sel_bin) == (kPickWords - 1) * 4,
+              "the pick is six consecutive words");
+
+// The filter's scratch, named at file scope so that the out-of-line threshold
+// search addresses it as shared memory (32-bit addresses, shared-memory
+// atomics) rather than through a generic pointer.
+__shared__ FilterScratch filter_scratch;
 
 __device__ __forceinline__ void clear_hist(FilterScratch& S, int nbins) {
   for (int i = threadIdx.x; i < nbins; i += kThreads) {
     S.cnt[i] = 0u;
-    S.massq[i] = 0ull;
+    S.mlo[i] = 0u;
+    S.mhi[i] = 0u;
     S.mass[i] = 0.f;
   }
 }
 
 __device__ __forceinline__ void fix_masses(FilterScratch& S, int nbins) {
   for (int i = threadIdx.x; i < nbins; i += kThreads)
-    if (S.massq[i]) S.mass[i] = (float)S.massq[i] * (1.0f / kMassUnit);
+    if (S.mlo[i] | S.mhi[i])
+      S.mass[i] = (float)(((unsigned long long)S.mhi[i] << 32) | S.mlo[i]) * (1.0f / kMassUnit);
+}
+
+// Add one id's mass (in (0, 1]) to a bin: the 32-bit low half with an atomic
+// that returns the old value, so the one add that wraps it carries into the
+// high half.  Native 32-bit atomics; a 64-bit shared-memory add loses far more
+// under contention (a pass where every id of a row lands in the window).
+__device__ __forceinline__ void add_mass(FilterScratch& S, int bin, float mass) {
+  const unsigned long long q = (unsigned long long)(mass * kMassUnit);
+  const uint32_t ql = (uint32_t)q, qh = (uint32_t)(q >> 32);
+  uint32_t carry = 0u;
+  if (ql) {
+    const uint32_t old = atomicAdd(&S.mlo[bin], ql);
+    carry = old + ql < old;
+  }
+  if (qh + carry) atomicAdd(&S.mhi[bin], qh + carry);
+}
+
+// A row is cut into `nrank` consecutive segments, one per CTA of a cluster,
+// and each CTA scans its segment into its own histogram.  Then:
+//   hist_merge   once every CTA has finished its scan (so rank 0's own
+//                shared-memory atomics are done), adds this CTA's non-empty
+//                bins into rank 0's histogram through distributed shared
+//                memory, and waits until every CTA has added;
+//   pick_share   after rank 0 has picked the bin: rank 0 writes the pick into
+//                the other CTAs' scratch, and all wait for it.
+// Every CTA of a cluster makes the same calls in the same order: the control
+// flow depends only on the row's statistics and on the picks, which all of the
+// cluster's CTAs hold alike.  With one CTA the calls do nothing.
+__device__ __forceinline__ void hist_merge(FilterScratch& S, int nbins, unsigned rank, unsigned nrank) {
+  if (nrank == 1) return;
+  cluster_arrive();
+  cluster_wait();                                   // every scan is done
+  if (rank != 0) {
+    for (int i = threadIdx.x; i < nbins; i += kThreads) {
+      const uint32_t c = S.cnt[i];
+      if (!c) continue;
+      cluster_red_add(cluster_map(&S.cnt[i], 0), c);
+      const uint32_t ql = S.mlo[i], qh = S.mhi[i];
+      uint32_t carry = 0u;
+      if (ql) {
+        const uint32_t old = cluster_atom_add(cluster_map(&S.mlo[i], 0), ql);
+        carry = old + ql < old;
+      }
+      if (qh + carry) cluster_red_add(cluster_map(&S.mhi[i], 0), qh + carry);
+    }
+  }
+  cluster_arrive();
+  cluster_wait();                                   // every CTA's bins are in
+}
+
+__device__ __forceinline__ void pick_share(FilterScratch& S, unsigned rank, unsigned nrank) {
+  if (nrank == 1) return;
+  const int t = threadIdx.x;
+  if (rank == 0 && t < (int)(nrank - 1) * kPickWords) {
+    const uint32_t* words = reinterpret_cast<const uint32_t*>(&S.sel_bin);
+    cluster_store(cluster_map(&words[t % kPickWords], 1 + t / kPickWords), words[t % kPickWords]);
+  }
+  cluster_arrive();
+  cluster_wait();
 }
 
 // Step 2's histogram over the ids with keys in [klo, khi], fed by scan_segment:
@@ -1011,22 +1130,36 @@ struct HistAcc {
       bin = (key >> shift_lo) & ((1u << (shift_hi - shift_lo)) - 1u);
     }
     atomicAdd(&S->cnt[bin], 1u);
-    atomicAdd(&S->massq[bin], (unsigned long long)(ex2_approx(fmaf(x, c, -mc)) * kMassUnit));
+    add_mass(*S, bin, ex2_approx(fmaf(x, c, -mc)));
   }
   template <typename TT, int U>
   __device__ __forceinline__ void vec(const uint4 (&v)[U], const int (&)[U]) {
 #pragma unroll
-    for (int u = 0; u < U; ++u)
+    for (int u = 0; u < U; ++u) {
+      if constexpr (U == kUnroll) {
+        // keys are ordered like the logits: a vector whose largest key lies
+        // below the range, or whose smallest lies above it, takes no part
+        float hi, lo;
+        vec_range<T>(v[u], hi, lo);
+        const bool slow = !(Keys<T>::of(hi) < klo || Keys<T>::of(lo) > khi);
+        warp_queue_ids<T>(*this, S->vq[threadIdx.x >> 5], v[u], slow);
+      } else {
 #pragma unroll
-      for (int e = 0; e < Vec<T>::n; ++e) elem(Vec<T>::at(v[u], e));
+        for (int e = 0; e < Vec<T>::n; ++e) elem(Vec<T>::at(v[u], e));
+      }
+    }
   }
   __device__ __forceinline__ void scalar(float x, int) { elem(x); }
 };
 
 // The bin where the count (by_mass false) or the mass, summed from the top
 // bin down, first reaches `need` (clamped to the total), with the count and
-// mass of the bins above it and of the bin itself.  All threads call it.
-__device__ void select_bin(FilterScratch& S, int nbins, bool by_mass, uint32_t need_cnt, float need_mass) {
+// mass of the bins above it and of the bin itself.  With `tail_unsummed`,
+// bin 0 is the window's tail, counted but without its mass: a mass target
+// above the other bins' total lies in the tail, and bin 0 is the pick.  All
+// threads call it.
+__device__ void select_bin(FilterScratch& S, int nbins, bool by_mass, bool tail_unsummed, uint32_t need_cnt,
+                           float need_mass) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int per = nbins >= kThreads ? nbins / kThreads : 1;
   const int owners = nbins / per;
@@ -1065,7 +1198,16 @@ __device__ void select_bin(FilterScratch& S, int nbins, bool by_mass, uint32_t n
   const uint32_t tc = S.wc[0];
   const float tm = S.wm[0];
   bool mine;
-  if (by_mass) {
+  if (by_mass && tail_unsummed && need_mass > tm && S.cnt[0] > 0u) {
+    mine = false;
+    if (t == 0) {
+      S.sel_bin = 0;
+      S.sel_cnt_above = tc - S.cnt[0];
+      S.sel_mass_above = tm;
+      S.sel_cnt_bin = S.cnt[0];
+      S.sel_mass_bin = 0.f;
+    }
+  } else if (by_mass) {
     const float need = fminf(need_mass, tm);
     mine = t < owners && lc > 0 && em < need && need <= im;
     if (!(tm > 0.f)) mine = t < owners && lc > 0 && ec + lc == tc;   // no mass seen: the lowest non-empty bin
@@ -1103,114 +1245,127 @@ __device__ void select_bin(FilterScratch& S, int nbins, bool by_mass, uint32_t n
   __syncthreads();
 }
 
-// Step 1's histogram for window `win`, fed by scan_segment.
-template <typename T>
+// Step 1's histogram for one window, fed by scan_segment (kFirst: window 0,
+// which has no earlier window above it).
+template <typename T, bool kFirst>
 struct DistAcc {
   FilterScratch* S;
-  uint32_t key_min;
-  float c, mc;
-  const Windows* W;
-  int win;
+  uint32_t key_min;   // ids with smaller keys take no part (0: every id)
+  float c, mc;        // mass = exp2(x c - mc) = exp((x - m) / T)
+  WinMap W;
   uint32_t tail_cnt;
-  float a0, b0;       // window 0's map, held in registers
+  // Above the window: nothing (an earlier window has it); in its tail:
+  // counted; else its bin takes the id's count and mass.
   __device__ __forceinline__ void elem(float x) {
-    if (win == 0) {
-      // the common pass: one FMA and a compare for an id far below the max
-      const float s = fmaf(-x, a0, b0);
-      if (!(s < (float)(kDistBins - 1))) {             // the tail, or -inf (s = +inf)
-        if (x > -CUDART_INF_F && (key_min == 0u || Keys<T>::of(x) >= key_min)) ++tail_cnt;
-        return;
-      }
-      if (key_min != 0u && Keys<T>::of(x) < key_min) return;
-      const int bin = (kDistBins - 1) - (int)fmaxf(s, 0.f);
-      atomicAdd(&S->cnt[bin], 1u);
-      atomicAdd(&S->massq[bin], (unsigned long long)(ex2_approx(fmaf(x, c, -mc)) * kMassUnit));
-      return;
-    }
-    if (!(x > -CUDART_INF_F)) return;
-    if (Keys<T>::of(x) < key_min) return;
-    const int bin = W->bin(x, win);
-    if (bin == kDistBins) return;                      // above the window: counted before
-    if (bin == 0) {                                    // the window's tail: counted only
+    if (!(x > -CUDART_INF_F)) return;                  // -inf ids are never kept
+    if (key_min != 0u && Keys<T>::of(x) < key_min) return;
+    if (!kFirst && W.above(x)) return;
+    const float s = fmaf(-x, W.a, W.b);
+    if (!(s < (float)(kDistBins - 1))) {
       ++tail_cnt;
       return;
     }
+    const int bin = (kDistBins - 1) - (int)fmaxf(s, 0.f);
     atomicAdd(&S->cnt[bin], 1u);
-    atomicAdd(&S->massq[bin], (unsigned long long)(ex2_approx(fmaf(x, c, -mc)) * kMassUnit));
+    add_mass(*S, bin, ex2_approx(fmaf(x, c, -mc)));
   }
   template <typename TT, int U>
   __device__ __forceinline__ void vec(const uint4 (&v)[U], const int (&)[U]) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      // window 0 without a key floor: a vector whose largest logit lies below
-      // the window and which holds no -inf is all tail (the window position is
-      // non-increasing in the logit, so this is the per-id test's answer).
-      // The other vectors go to the warp's queue, and the warp's lanes share
-      // their ids out, so the per-id test runs with every lane busy.  Only
-      // scan_segment's full batches (U == kUnroll) come here: every thread of
-      // the CTA takes part in them, as the warp-wide ballot and syncs need; its
-      // remainder loop, where a warp may be partly idle, takes the per-id test.
-      if (U == kUnroll && win == 0 && key_min == 0u) {
+      if constexpr (U == kUnroll) {
+        // the window's position and the key are monotone in the logit, so the
+        // largest and smallest logit decide for the whole vector when: every
+        // id lies below key_min or above the window (nothing to do), or every
+        // id takes part and lies in the window's tail (counted at once)
         float hi, lo;
-        if constexpr (sizeof(T) == 2) {
-          const uint32_t mx = bf16x2_nanmax(bf16x2_nanmax(v[u].x, v[u].y), bf16x2_nanmax(v[u].z, v[u].w));
-          const uint32_t mn = bf16x2_min(bf16x2_min(v[u].x, v[u].y), bf16x2_min(v[u].z, v[u].w));
-          hi = fmaxf(bf16_lo(mx), bf16_hi(mx));
-          lo = fminf(bf16_lo(mn), bf16_hi(mn));
-        } else {
-          hi = fmaxf(fmaxf(__uint_as_float(v[u].x), __uint_as_float(v[u].y)),
-                     fmaxf(__uint_as_float(v[u].z), __uint_as_float(v[u].w)));
-          lo = fminf(fminf(__uint_as_float(v[u].x), __uint_as_float(v[u].y)),
-                     fminf(__uint_as_float(v[u].z), __uint_as_float(v[u].w)));
-        }
-        const bool all_tail = lo > -CUDART_INF_F && !(fmaf(-hi, a0, b0) < (float)(kDistBins - 1));
-        if (all_tail) tail_cnt += Vec<T>::n;
-        const int lane = threadIdx.x & 31;
-        const unsigned slow = __ballot_sync(0xffffffffu, !all_tail);
-        if (!slow) continue;
-        uint4* q = S->vq[threadIdx.x >> 5];
-        if (!all_tail) q[__popc(slow & ((1u << lane) - 1u))] = v[u];
-        __syncwarp();
-        const int n = __popc(slow) * Vec<T>::n;
-        for (int i = lane; i < n; i += 32) elem(Vec<T>::at(q[i / Vec<T>::n], i % Vec<T>::n));
-        __syncwarp();                    // the queue is refilled by the next vector
-        continue;
-      }
+        vec_range<T>(v[u], hi, lo);
+        const bool none = (key_min != 0u && Keys<T>::of(hi) < key_min) || (!kFirst && W.above(lo));
+        const bool tail = lo > -CUDART_INF_F && (key_min == 0u || Keys<T>::of(lo) >= key_min) &&
+                          !(fmaf(-hi, W.a, W.b) < (float)(kDistBins - 1));
+        if (!none && tail) tail_cnt += Vec<T>::n;
+        warp_queue_ids<T>(*this, S->vq[threadIdx.x >> 5], v[u], !none && !tail);
+      } else {
 #pragma unroll
-      for (int e = 0; e < Vec<T>::n; ++e) elem(Vec<T>::at(v[u], e));
+        for (int e = 0; e < Vec<T>::n; ++e) elem(Vec<T>::at(v[u], e));
+      }
     }
   }
   __device__ __forceinline__ void scalar(float x, int) { elem(x); }
 };
 
+// The smallest k in [l, h) with pred(k), else h, for a predicate that is
+// false and then true over the range.  All threads call it: each round tests
+// kThreads evenly spaced keys at once and keeps the one gap that holds the
+// change (two rounds for 16-bit keys, four or five for 32-bit ones).
+template <class Pred>
+__device__ uint32_t first_true(uint32_t l, uint32_t h, Pred pred) {
+  while (l < h) {
+    const uint64_t step = ((uint64_t)(h - l) + kThreads - 1) / kThreads;
+    const uint64_t q = (uint64_t)l + (uint64_t)threadIdx.x * step;
+    const int f = __syncthreads_count(q < h && !pred((uint32_t)q));
+    if (f == 0) return l;
+    // tests 0..f-1 false, test f (where it lies below h) true
+    const uint64_t nh = (uint64_t)l + (uint64_t)f * step;
+    l = (uint32_t)((uint64_t)l + (uint64_t)(f - 1) * step + 1);
+    if (nh < h) h = (uint32_t)nh;
+  }
+  return h;
+}
+
 // The largest key whose count (by_mass false) or mass of ids at or above it,
 // among the ids with key >= key_min, reaches the target.  Returns false when
-// the count target is at least the number of those ids (no threshold).  Kept
-// out of line: the filter calls it twice (top-k, then top-p), and one copy of
-// its histogram loops instead of two cut the filter's instruction-fetch
-// stalls (measured 118.4 -> 94.5 us on C3 with top-p 0.8).
+// the count target is at least the number of those ids (no threshold).
+// `reuse_w0`: the scratch already holds window 0's histogram of every id of
+// the row (a previous call left it, `left_w0`); ids with keys below key_min
+// then sit in bins below the target's, so the first pass is not repeated.
+// Kept out of line: the filter calls it twice (top-k, then top-p), and one
+// copy of its histogram loops instead of two cut the filter's
+// instruction-fetch stalls (measured 118.4 -> 94.5 us on C3 with top-p 0.8).
 template <typename T>
-__device__ __noinline__ bool find_threshold(const T* row, const Params& P, const RowStat& rs, FilterScratch& S, bool by_mass,
-                               uint32_t need_cnt, float need_mass, uint32_t key_min, uint32_t& key, float& mass_ge) {
+__device__ __noinline__ bool find_threshold(const T* row, int e0, int e1, unsigned rank, unsigned nrank, const Params& P,
+                                            const RowStat& rs, bool by_mass, uint32_t need_cnt, float need_mass,
+                                            uint32_t key_min, bool reuse_w0, uint32_t& key, float& mass_ge,
+                                            bool& left_w0) {
+  FilterScratch& S = filter_scratch;
+  left_w0 = false;
   // step 1: the distance bin, window by window until the target falls in a bin
   uint32_t cnt_above = 0;
   float mass_above = 0.f, bin_mass = 0.f;
   int win = 0, dbin = 0;
-  const Windows W(rs.m, P.invT);
   for (; win < kWindows; ++win) {
-    clear_hist(S, kDistBins);
-    __syncthreads();
-    DistAcc<T> da{&S, key_min, P.c, rs.m * P.c, &W, win, 0u, W.a[0], W.b[0]};
-    scan_segment<T>(row, 0, P.V, da);
-    const uint32_t tc = __reduce_add_sync(0xffffffffu, da.tail_cnt);
-    if ((threadIdx.x & 31) == 0 && tc) atomicAdd(&S.cnt[0], tc);
-    __syncthreads();
-    fix_masses(S, kDistBins);
-    __syncthreads();
-    // the tail's mass is not summed: a mass target beyond the bins clamps to
-    // their total and lands on the tail, and the next window takes it up
-    select_bin(S, kDistBins, by_mass, need_cnt - cnt_above, need_mass - mass_above);
-    if (win == 0 && !by_mass && S.total_cnt <= need_cnt) return false;
+    if (win > 0 || !reuse_w0) {
+      clear_hist(S, kDistBins);
+      __syncthreads();
+      uint32_t tail = 0;
+      if (win == 0) {
+        DistAcc<T, true> da{&S, key_min, P.c, rs.m * P.c, WinMap(rs.m, P.invT, 0), 0u};
+        scan_segment<T>(row, e0, e1, da);
+        tail = da.tail_cnt;
+      } else {
+        DistAcc<T, false> da{&S, key_min, P.c, rs.m * P.c, WinMap(rs.m, P.invT, win), 0u};
+        scan_segment<T>(row, e0, e1, da);
+        tail = da.tail_cnt;
+      }
+      const uint32_t tc = __reduce_add_sync(0xffffffffu, tail);
+      if ((threadIdx.x & 31) == 0 && tc) atomicAdd(&S.cnt[0], tc);
+      __syncthreads();
+      hist_merge(S, kDistBins, rank, nrank);
+      if (rank == 0) {
+        fix_masses(S, kDistBins);
+        __syncthreads();
+      }
+    }
+    if (rank == 0) {
+      // the tail's mass is not summed: a mass target beyond the other bins'
+      // total lands on the tail, and the next window takes it up
+      select_bin(S, kDistBins, by_mass, true, need_cnt - cnt_above, need_mass - mass_above);
+    }
+    pick_share(S, rank, nrank);
+    if (win == 0 && !by_mass && S.total_cnt <= need_cnt) {
+      left_w0 = key_min == 0u;
+      return false;
+    }
     dbin = S.sel_bin;
     cnt_above += S.sel_cnt_above;
     mass_above += S.sel_mass_above;
@@ -1220,31 +1375,17 @@ __device__ __noinline__ bool find_threshold(const T* row, const Params& P, const
   }
   if (win == kWindows) win = kWindows - 1;
   // the bin's key range: its position is non-decreasing in the key over the
-  // finite values up to the max
-  if (threadIdx.x == 0) {
-    auto ord = [&](uint32_t k) { return W.bin(Keys<T>::value(k), win); };
-    uint32_t a = Keys<T>::of(-CUDART_INF_F) + 1, z = Keys<T>::of(rs.m);
-    if (a < key_min) a = key_min;
-    uint32_t l = a, h = z;                            // smallest key at or above the bin
-    while (l < h) {
-      const uint32_t mid = l + (h - l) / 2;
-      if (ord(mid) >= dbin) h = mid; else l = mid + 1;
-    }
-    uint32_t l2 = l, h2 = z;                          // largest key at or below it
-    while (l2 < h2) {
-      const uint32_t mid = l2 + (h2 - l2 + 1) / 2;
-      if (ord(mid) <= dbin) l2 = mid; else h2 = mid - 1;
-    }
-    S.wc[0] = l;
-    S.wc[1] = l2;
-  }
-  __syncthreads();
-  const uint32_t lo = S.wc[0], hi = S.wc[1];
-  __syncthreads();
+  // finite values up to the max (whose key + 1 does not overflow)
+  const WinMap W(rs.m, P.invT, win);
+  const uint32_t z = Keys<T>::of(rs.m);
+  const uint32_t a = max(Keys<T>::of(-CUDART_INF_F) + 1, key_min);
+  const uint32_t lo = first_true(a, z, [&](uint32_t k) { return W.bin(Keys<T>::value(k)) >= dbin; });
+  const uint32_t hi = first_true(lo + 1, z + 1, [&](uint32_t k) { return W.bin(Keys<T>::value(k)) > dbin; }) - 1;
   if (dbin > 0 && lo == hi) {
     // one key in the bin (the usual case near the top): step 1 has it all
     key = lo;
     mass_ge = mass_above + bin_mass;
+    left_w0 = win == 0 && key_min == 0u;
     return true;
   }
   // step 2: the exact key among the ids of that bin
@@ -1261,11 +1402,15 @@ __device__ __noinline__ bool find_threshold(const T* row, const Params& P, const
     acc.prefix = prefix;
     acc.shift_hi = kBits - decided;
     acc.shift_lo = kBits - decided - w;
-    scan_segment<T>(row, 0, P.V, acc);
+    scan_segment<T>(row, e0, e1, acc);
     __syncthreads();
-    fix_masses(S, nbins);
-    __syncthreads();
-    select_bin(S, nbins, by_mass, need_cnt - cnt_above, need_mass - mass_above);
+    hist_merge(S, nbins, rank, nrank);
+    if (rank == 0) {
+      fix_masses(S, nbins);
+      __syncthreads();
+      select_bin(S, nbins, by_mass, false, need_cnt - cnt_above, need_mass - mass_above);
+    }
+    pick_share(S, rank, nrank);
     if (acc.one_round) {
       prefix = lo + (uint32_t)S.sel_bin;
     } else {
@@ -1282,15 +1427,21 @@ __device__ __noinline__ bool find_threshold(const T* row, const Params& P, const
   return true;
 }
 
-// One CTA per row: its threshold and kept mass; the CTA that filters a
-// sequence's last row runs the sequence's accept scan on the filtered rows.
+// One cluster per row (filter_cluster_ctas CTAs, each scanning one segment
+// of the row into its own histograms, merged at rank 0): the row's threshold
+// and kept mass; the cluster that filters a sequence's last row runs the
+// sequence's accept scan on the filtered rows.
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 6) filter_kernel(const Params P) {
-  __shared__ FilterScratch S;
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // the row pass's statistics must be visible
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const long long r = blockIdx.x;
+  const unsigned rank = cluster_rank(), nrank = cluster_ctas();
+  const long long r = blockIdx.x / nrank;
+  // segments of whole batches of 16-byte vectors (the last one shorter)
+  constexpr int kBatchElems = kUnroll * kThreads * Vec<T>::n;
+  const int per = (int)(((P.V + kBatchElems - 1) / kBatchElems + nrank - 1) / nrank) * kBatchElems;
+  const int e0 = min(P.V, (int)rank * per), e1 = min(P.V, e0 + per);
   int b;
   const T* row = row_ptr<T, kStochastic>(P, r, b);
   const RowStat rs = ldcg_stat(P.ws.row_stat + r);
@@ -1298,18 +1449,22 @@ __global__ void __launch_bounds__(kThreads, 6) filter_kernel(const Params P) {
   if (rs.status == SPEC_OK) {
     float mass = __expf(rs.lnS);                       // the row's mass relative to its max
     uint32_t key = 0, key_min = 0;
-    bool thr = false;
+    bool thr = false, w0 = false;
     if (P.top_k > 0) {
       float mk;
-      if (find_threshold<T>(row, P, rs, S, false, (uint32_t)P.top_k, 0.f, 0u, key, mk)) {
+      if (find_threshold<T>(row, e0, e1, rank, nrank, P, rs, false, (uint32_t)P.top_k, 0.f, 0u, false, key, mk, w0)) {
         thr = true;
         mass = mk;
         key_min = key;
       }
     }
     if (P.top_p > 0.f && P.top_p < 1.f) {
+      // top-p on the top-k ids: when the top-k pass ended on window 0's
+      // histogram, the kept ids are that histogram's bins from the top down to
+      // the top-k key's, and the top-p target lies among them
       float mp;
-      find_threshold<T>(row, P, rs, S, true, 0u, P.top_p * mass, key_min, key, mp);
+      bool unused;
+      find_threshold<T>(row, e0, e1, rank, nrank, P, rs, true, 0u, P.top_p * mass, key_min, w0, key, mp, unused);
       thr = true;
       mass = mp;
     }
@@ -1318,7 +1473,7 @@ __global__ void __launch_bounds__(kThreads, 6) filter_kernel(const Params P) {
       lnM = logf(mass);
     }
   }
-  if (threadIdx.x < 32) {
+  if (rank == 0 && threadIdx.x < 32) {
     int last = 0;
     if (threadIdx.x == 0) {
       __stcg(P.ws.row_filter + r, make_float2(tau, lnM));
@@ -1900,6 +2055,19 @@ static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_
 // as replays of a captured graph, a call finds the workspace all zero -- as
 // it was first handed over -- and needs no clearing.
 
+// CTAs per row in the filter (a cluster; the kernel takes any size up to the
+// portable 8).  Measured on 64 x 17 rows of 128256 bf16 logits: a row's first
+// pass streams at the same rate cut or whole, and every CTA of a cut row pays
+// the merge and waits for the pick, so top-p alone is fastest whole (98.8 us;
+// 2 CTAs 107, 4 CTAs 137).  A top-k target below window 0 (rows whose max
+// stands far above the rest) takes two more passes over its row, at the end
+// of the launch; two CTAs halve those (top-k 50: 222 -> 179 us; with top-p
+// 0.8: 245 -> 203 us).  So rows of 128 KB or more take two CTAs when a top-k
+// stage runs.
+static int filter_cluster_ctas(int V, size_t esize, int top_k) {
+  return top_k > 0 && (long long)V * (long long)esize >= 131072 ? 2 : 1;
+}
+
 // Resident CTAs of a kernel with `threads` threads and `smem` bytes of dynamic
 // shared memory on the current device, cached per (device, kernel).
 static int resident_ctas(const void* fn, size_t smem = 0, int threads = kThreads) {
@@ -1966,12 +2134,20 @@ static int launch(Params& P, cudaStream_t stream, const spec_verify_aux* aux) {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     if (P.filtering) {
+      const int fc = filter_cluster_ctas(P.V, sizeof(T), P.top_k);
+      if (P.R * fc > (long long)INT_MAX) return SPEC_ERR_UNSUPPORTED;
+      cudaLaunchAttribute fattr[2];
+      fattr[0] = attr[0];
+      fattr[1].id = cudaLaunchAttributeClusterDimension;
+      fattr[1].val.clusterDim.x = (unsigned)fc;
+      fattr[1].val.clusterDim.y = 1;
+      fattr[1].val.clusterDim.z = 1;
       cudaLaunchConfig_t fcfg = {};
-      fcfg.gridDim = dim3((unsigned)P.R);
+      fcfg.gridDim = dim3((unsigned)(P.R * fc));
       fcfg.blockDim = dim3(kThreads);
       fcfg.stream = stream;
-      fcfg.attrs = attr;
-      fcfg.numAttrs = 1;
+      fcfg.attrs = fattr;
+      fcfg.numAttrs = fc > 1 ? 2 : 1;
       if (cudaLaunchKernelEx(&fcfg, filter_kernel<T>, P) != cudaSuccess) return SPEC_ERR_CUDA;
     }
     if (rec(2) != cudaSuccess) return SPEC_ERR_CUDA;

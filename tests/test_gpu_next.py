@@ -238,6 +238,49 @@ def test_filtered_ties_and_masked_vocabulary(sv):
         _filtered(sv, w, 31, top_k, top_p)
 
 
+def _cluster_ctas(V, esize, top_k):
+    """The filter's CTAs per row: two when a top-k stage runs on rows of 128 KB or more."""
+    return 2 if top_k > 0 and V * esize >= 131072 else 1
+
+
+def _segments(V, esize, c):
+    """The element ranges the cluster's CTAs scan (whole 1024-vector batches)."""
+    batch = 4 * 256 * (16 // esize)
+    per = -(-(-(-V // batch)) // c) * batch
+    return [(min(V, r * per), min(V, r * per + per)) for r in range(c)]
+
+
+@pytest.mark.parametrize("dtype,V,ties", [
+    (wl.BF16, 151937, False),     # rows not 16-byte aligned (odd V)
+    (wl.BF16, 151937, True),      # the same with heavy ties across the segments
+    (wl.FP32, 114689, False),
+    (wl.FP32, 40000, True),       # 160 KB rows, the second segment short and ragged
+    (wl.BF16, 49153, False),      # rows under 128 KB: one CTA each
+])
+def test_filtered_rows_cut_across_a_cluster(sv, dtype, V, ties):
+    """Rows cut into segments scanned by the CTAs of a cluster (top-k stages on
+    long rows), their histograms merged through distributed shared memory:
+    thresholds found in the first window, in the coarser windows (top-k far
+    below the max) and by the exact key passes, and top-p after top-k on the
+    first window's histogram."""
+    esize = 2 if dtype == wl.BF16 else 4
+    w = wl.gaussian_pair(3, 3, V, dtype, 0.8, seed=V % 97 + ties, sigma_t=4.0, sigma_d=1.0)
+    if ties:
+        rng = np.random.default_rng(5)
+        t = np.round(wl.logits_as_f32(w.target, dtype) * 2) / 2
+        t[:, :, rng.random(V) < 0.1] = -np.inf
+        d = t[:, :w.k] + np.round(rng.normal(size=t[:, :w.k].shape)) / 2
+        w = wl.Workload("ties", "stochastic", w.B, w.k, V, dtype, w.temperature, wl.store(t.astype(np.float32), dtype),
+                        wl.store(d.astype(np.float32), dtype), np.argmax(d, axis=-1).astype(np.int32))
+    cut = 0
+    for top_k, top_p in [(0, 0.8), (V // 2, 0.0), (V // 3, 0.95), (37, 0.0), (37, 0.9), (0, 0.999)]:
+        c = _cluster_ctas(V, esize, top_k)
+        assert _segments(V, esize, c)[-1][1] == V
+        cut += c > 1
+        _filtered(sv, w, 41 + top_k, top_k, top_p)
+    assert cut == (0 if V * esize < 131072 else 4)
+
+
 def test_filtering_is_ignored_in_greedy_mode(sv):
     w = wl.c4(0.8, seed=3, B=4, k=6, V=2000)
     t, x = to_device(w.target, w.dtype), tokens_to_device(w.tokens)
