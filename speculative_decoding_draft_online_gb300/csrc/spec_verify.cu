@@ -990,21 +990,32 @@ __device__ __forceinline__ void vec_range(const uint4& v, float& hi, float& lo) 
 
 // The histogram passes test each 16-byte vector first (from its largest and
 // smallest logit): most vectors take no part or are counted whole.  The rest
-// go through the warp's queue, and the warp's lanes share their ids out, so
-// the per-id test runs with every lane busy.  Only scan_segment's full batches
-// come here: every thread of the CTA takes part in them, as the warp-wide
-// ballot and syncs need; its remainder loop, where a warp may be partly idle,
-// tests every id.
-template <typename T, class Acc>
-__device__ __forceinline__ void warp_queue_ids(Acc& acc, uint4* q, const uint4& v, bool slow) {
+// of a batch go into the warp's queue, and then the warp's lanes share their
+// ids out, so the per-id test runs with every lane busy, one queue run (two
+// warp syncs) per batch.  Only scan_segment's full batches come here: every
+// thread of the CTA takes part in them, as the warp-wide ballot and syncs
+// need; its remainder loop, where a warp may be partly idle, tests every id.
+// The queues (a batch's vectors for each warp, 32 KB) leave room for four CTAs
+// per SM, at up to 64 registers; a queue run per vector (4 KB of queues, six
+// CTAs of 40 registers) took 94.9 us for top-p 0.8 on 64 x 17 rows of 128256
+// bf16 logits, against 86.0 us now.
+// Queue one vector of a batch (slow: it needs the per-id test); `fill` counts
+// the warp's queued vectors.
+__device__ __forceinline__ void warp_queue_put(uint4* q, int& fill, const uint4& v, bool slow) {
   const int lane = threadIdx.x & 31;
   const unsigned m = __ballot_sync(0xffffffffu, slow);
-  if (!m) return;
-  if (slow) q[__popc(m & ((1u << lane) - 1u))] = v;
+  if (slow) q[fill + __popc(m & ((1u << lane) - 1u))] = v;
+  fill += __popc(m);
+}
+// Run the per-id test on the batch's queued vectors, the lanes sharing the ids.
+template <typename T, class Acc>
+__device__ __forceinline__ void warp_queue_run(Acc& acc, const uint4* q, int fill) {
+  if (!fill) return;
+  const int lane = threadIdx.x & 31;
   __syncwarp();
-  const int n = __popc(m) * Vec<T>::n;
+  const int n = fill * Vec<T>::n;
   for (int i = lane; i < n; i += 32) acc.elem(Vec<T>::at(q[i / Vec<T>::n], i % Vec<T>::n));
-  __syncwarp();                          // the queue is refilled by the next vector
+  __syncwarp();                          // the queue is refilled by the next batch
 }
 
 constexpr float kMassUnit = 1099511627776.0f;   // 2^40: fixed-point scale of a mass in (0, 1]
@@ -1017,7 +1028,7 @@ struct FilterScratch {
   uint32_t mlo[kHistBins], mhi[kHistBins];
   uint32_t wc[kWarps];
   float wm[kWarps];
-  uint4 vq[kWarps][32];                  // per warp: 16-byte vectors that need the per-id test
+  uint4 vq[kWarps][kUnroll * 32];        // per warp: a batch's 16-byte vectors that need the per-id test
   // select_bin's result (six words, sent to the cluster's other CTAs as such)
   int sel_bin;
   uint32_t sel_cnt_above, sel_cnt_bin, total_cnt;
@@ -1134,19 +1145,23 @@ struct HistAcc {
   }
   template <typename TT, int U>
   __device__ __forceinline__ void vec(const uint4 (&v)[U], const int (&)[U]) {
+    if constexpr (U == kUnroll) {
+      uint4* q = S->vq[threadIdx.x >> 5];
+      int fill = 0;
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      if constexpr (U == kUnroll) {
+      for (int u = 0; u < U; ++u) {
         // keys are ordered like the logits: a vector whose largest key lies
         // below the range, or whose smallest lies above it, takes no part
         float hi, lo;
         vec_range<T>(v[u], hi, lo);
-        const bool slow = !(Keys<T>::of(hi) < klo || Keys<T>::of(lo) > khi);
-        warp_queue_ids<T>(*this, S->vq[threadIdx.x >> 5], v[u], slow);
-      } else {
+        warp_queue_put(q, fill, v[u], !(Keys<T>::of(hi) < klo || Keys<T>::of(lo) > khi));
+      }
+      warp_queue_run<T>(*this, q, fill);
+    } else {
+#pragma unroll
+      for (int u = 0; u < U; ++u)
 #pragma unroll
         for (int e = 0; e < Vec<T>::n; ++e) elem(Vec<T>::at(v[u], e));
-      }
     }
   }
   __device__ __forceinline__ void scalar(float x, int) { elem(x); }
@@ -1271,9 +1286,11 @@ struct DistAcc {
   }
   template <typename TT, int U>
   __device__ __forceinline__ void vec(const uint4 (&v)[U], const int (&)[U]) {
+    if constexpr (U == kUnroll) {
+      uint4* q = S->vq[threadIdx.x >> 5];
+      int fill = 0;
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      if constexpr (U == kUnroll) {
+      for (int u = 0; u < U; ++u) {
         // the window's position and the key are monotone in the logit, so the
         // largest and smallest logit decide for the whole vector when: every
         // id lies below key_min or above the window (nothing to do), or every
@@ -1284,11 +1301,14 @@ struct DistAcc {
         const bool tail = lo > -CUDART_INF_F && (key_min == 0u || Keys<T>::of(lo) >= key_min) &&
                           !(fmaf(-hi, W.a, W.b) < (float)(kDistBins - 1));
         if (!none && tail) tail_cnt += Vec<T>::n;
-        warp_queue_ids<T>(*this, S->vq[threadIdx.x >> 5], v[u], !none && !tail);
-      } else {
+        warp_queue_put(q, fill, v[u], !none && !tail);
+      }
+      warp_queue_run<T>(*this, q, fill);
+    } else {
+#pragma unroll
+      for (int u = 0; u < U; ++u)
 #pragma unroll
         for (int e = 0; e < Vec<T>::n; ++e) elem(Vec<T>::at(v[u], e));
-      }
     }
   }
   __device__ __forceinline__ void scalar(float x, int) { elem(x); }
@@ -1432,7 +1452,7 @@ __device__ __noinline__ bool find_threshold(const T* row, int e0, int e1, unsign
 // and kept mass; the cluster that filters a sequence's last row runs the
 // sequence's accept scan on the filtered rows.
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 6) filter_kernel(const Params P) {
+__global__ void __launch_bounds__(kThreads, 4) filter_kernel(const Params P) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // the row pass's statistics must be visible
   asm volatile("griddepcontrol.wait;" ::: "memory");
