@@ -78,10 +78,19 @@ struct Partial {
   int pad;
 };
 
+// A sequence's state after its accept scan, and what the sampling pass needs
+// of its sampled row, in one 32-byte record: a sampling CTA has all of it
+// after one load and issues its copies at once.
 struct SeqState {
   int n;
   int status;
+  int ft;                // residual: first tile of the piece holding the target row's max
+  float tau_d;           // residual, filtering: the draft's kept set is x_d >= tau_d (-inf: all)
+  float mt, lnSt;        // residual: target row max and ln of its (kept) mass relative to the max
+  float cdelta;          // residual: delta_v = fma(x_d - x_t, 1/T, cdelta)
+  float tau_t;           // filtering: the sampled row's kept set is x_t >= tau_t (-inf: all)
 };
+static_assert(sizeof(SeqState) == 32, "one 32-byte record a sequence");
 
 struct Workspace {
   Partial* row_partial;    // [R][nt]
@@ -346,18 +355,32 @@ __device__ void accept_scan(const Params& P, int b) {
   const long long obase = (long long)b * 2 * k;   // [B][2k] lse output
   int n = k;
   unsigned tok_bad = 0, nf_bad = 0, to_bad = 0;
+  // the sampled row's record: the rejected position's rows (set below), or the bonus row's filter
+  SeqState rec{0, 0, 0, -CUDART_INF_F, 0.f, 0.f, 0.f, -CUDART_INF_F};
   for (int base = 0; base < k; base += 32) {
     const int i = base + lane;
     const bool valid = i < k;
     bool acc = true;
     bool tbad = false, fbad = false, tmo = false;
+    SeqState mine{0, 0, 0, -CUDART_INF_F, 0.f, 0.f, 0.f, -CUDART_INF_F};   // this lane's position as the sampled one
     if (valid) {
       const int x = P.tokens[(size_t)b * k + i];
       const RowStat rt = ldcg_stat(P.ws.row_stat + rbase + i);
       const RowStat rd = ldcg_stat(P.ws.row_stat + rbase + k + i);
+      float2 ft = make_float2(-CUDART_INF_F, rt.lnS), fd = make_float2(-CUDART_INF_F, rd.lnS);
+      if (P.filtering) {
+        ft = __ldcg(P.ws.row_filter + rbase + i);
+        fd = __ldcg(P.ws.row_filter + rbase + k + i);
+      }
       fbad = rt.status != SPEC_OK || rd.status != SPEC_OK;
       tmo = rt.status == SPEC_ERR_TIMEOUT || rd.status == SPEC_ERR_TIMEOUT;
       tbad = x < 0 || x >= P.V;
+      mine.ft = rt.arg >= 0 && rt.arg < P.nt ? rt.arg : 0;
+      mine.tau_d = fd.x;
+      mine.mt = rt.m;
+      mine.lnSt = ft.y;
+      mine.cdelta = -(rd.m - rt.m) * P.invT - (fd.y - ft.y);
+      mine.tau_t = ft.x;
       if (!tbad) {
         const float xt = load_elem<T>((const T*)P.target, ((size_t)b * (k + 1) + i) * P.V + x);
         const float xd = load_elem<T>((const T*)P.draft, ((size_t)b * k + i) * P.V + x);
@@ -365,8 +388,6 @@ __device__ void accept_scan(const Params& P, int b) {
         float lq = (xd - rd.m) * P.invT - rd.lnS;          // ln q_i(x_i)
         if (P.filtering) {
           // the filtered, renormalised rows: 0 outside the kept set
-          const float2 ft = __ldcg(P.ws.row_filter + rbase + i);
-          const float2 fd = __ldcg(P.ws.row_filter + rbase + k + i);
           lp = xt >= ft.x ? (xt - rt.m) * P.invT - ft.y : -CUDART_INF_F;
           lq = xd >= fd.x ? (xd - rd.m) * P.invT - fd.y : -CUDART_INF_F;
         }
@@ -385,17 +406,30 @@ __device__ void accept_scan(const Params& P, int b) {
     nf_bad |= __ballot_sync(0xffffffffu, fbad);
     to_bad |= __ballot_sync(0xffffffffu, tmo);
     const unsigned rej = __ballot_sync(0xffffffffu, valid && !acc);
-    if (n == k && rej) n = base + __ffs(rej) - 1;
+    if (n == k && rej) {
+      n = base + __ffs(rej) - 1;
+      const int src = n - base;
+      rec.ft = __shfl_sync(0xffffffffu, mine.ft, src);
+      rec.tau_d = __shfl_sync(0xffffffffu, mine.tau_d, src);
+      rec.mt = __shfl_sync(0xffffffffu, mine.mt, src);
+      rec.lnSt = __shfl_sync(0xffffffffu, mine.lnSt, src);
+      rec.cdelta = __shfl_sync(0xffffffffu, mine.cdelta, src);
+      rec.tau_t = __shfl_sync(0xffffffffu, mine.tau_t, src);
+    }
   }
   // filtering runs over every row of the sequence, the bonus row included
   if (P.filtering) {
     const int bs = ldcg_stat(P.ws.row_stat + rbase + 2 * k).status;
     if (bs != SPEC_OK) nf_bad = 1;
     if (bs == SPEC_ERR_TIMEOUT) to_bad = 1;
+    if (n == k) rec.tau_t = __ldcg(P.ws.row_filter + rbase + 2 * k).x;   // the bonus row's filter
   }
   if (lane == 0) {
-    const int st = tok_bad ? SPEC_ERR_TOKEN : to_bad ? SPEC_ERR_TIMEOUT : nf_bad ? SPEC_ERR_NONFINITE : SPEC_OK;
-    __stcg(reinterpret_cast<int2*>(P.ws.seq) + b, make_int2(n, st));
+    rec.n = n;
+    rec.status = tok_bad ? SPEC_ERR_TOKEN : to_bad ? SPEC_ERR_TIMEOUT : nf_bad ? SPEC_ERR_NONFINITE : SPEC_OK;
+    int4* dst = reinterpret_cast<int4*>(P.ws.seq + b);
+    __stcg(dst, make_int4(rec.n, rec.status, rec.ft, __float_as_int(rec.tau_d)));
+    __stcg(reinterpret_cast<float4*>(dst + 1), make_float4(rec.mt, rec.lnSt, rec.cdelta, rec.tau_t));
   }
 }
 
@@ -1761,8 +1795,10 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const Params P) {
   const int b = blockIdx.x / P.ns;
   const int c = blockIdx.x % P.ns;
   const int k = P.k;
-  const int2 sv2 = __ldcg(reinterpret_cast<const int2*>(P.ws.seq) + b);
-  const int n = sv2.x, status = sv2.y;
+  // the sequence's record: n, status and the sampled row's statistics at once
+  const int4 q0 = __ldcg(reinterpret_cast<const int4*>(P.ws.seq + b));
+  const float4 q1 = __ldcg(reinterpret_cast<const float4*>(P.ws.seq + b) + 1);
+  const int n = q0.x, status = q0.y;
   const bool active = status == SPEC_OK;            // uniform over the CTA
   Draw D;
   D.invT = P.invT;
@@ -1795,31 +1831,20 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const Params P) {
     bulk_copy_g2s(S.tile[s][0], trow + v0, bytes, &S.bar[s]);
     if (drow) bulk_copy_g2s(S.tile[s][1], drow + v0, bytes, &S.bar[s]);
   };
-  __syncthreads();                                   // barriers initialised
-  // the CTA's own tiles do not depend on the floor tile: start them now
-  if (bulk && threadIdx.x == 0)
-    for (int i = D.R.resid ? 1 : 0; i < min(m, kStages); ++i) issue(i);
-  if (active && !D.R.resid && P.filtering)
-    D.R.tau_t = __ldcg(P.ws.row_filter + (long long)b * P.rows_per_seq + 2 * k).x;   // the bonus row's filter
-  if (active && D.R.resid) {
-    const long long rt_i = (long long)b * P.rows_per_seq + n;
-    const RowStat rt = ldcg_stat(P.ws.row_stat + rt_i);
-    const RowStat rd = ldcg_stat(P.ws.row_stat + rt_i + k);
-    float lnSt = rt.lnS, lnSd = rd.lnS;
-    if (P.filtering) {
-      const float2 ft2 = __ldcg(P.ws.row_filter + rt_i);
-      const float2 fd2 = __ldcg(P.ws.row_filter + rt_i + k);
-      D.R.tau_t = ft2.x;
-      D.R.tau_d = fd2.x;
-      lnSt = ft2.y;
-      lnSd = fd2.y;
+  if (active) {
+    D.R.tau_t = q1.w;                                // filtering: the sampled row's kept set
+    if (D.R.resid) {
+      D.R.mt = q1.x;
+      D.R.lnSt = q1.y;
+      D.R.cdelta = q1.z;
+      D.R.tau_d = __int_as_float(q0.w);
+      ft = q0.z >= 0 && q0.z < P.nt ? q0.z : 0;       // the first tile of the piece holding the row's max
     }
-    D.R.mt = rt.m;
-    D.R.lnSt = lnSt;
-    D.R.cdelta = -(rd.m - rt.m) * P.invT - (lnSd - lnSt);
-    ft = rt.arg >= 0 && rt.arg < P.nt ? rt.arg : 0;   // the first tile of the piece holding the row's max
-    if (bulk && threadIdx.x == 0) issue(0);
   }
+  __syncthreads();                                   // barriers initialised
+  // the floor tile first, then the CTA's own tiles
+  if (bulk && threadIdx.x == 0)
+    for (int i = 0; i < min(m, kStages); ++i) issue(i);
   uint32_t* queue = S.queue[threadIdx.x >> 5];
 
   float floor = -CUDART_INF_F, best = -CUDART_INF_F;
@@ -1962,7 +1987,10 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const Params P) {
       stcg_stat(P.ws.row_stat + rb + r, RowStat{0.f, 0.f, 0, 0});
       if (P.filtering) __stcg(P.ws.row_filter + rb + r, make_float2(0.f, 0.f));
     }
-    if (threadIdx.x == 0) __stcg(reinterpret_cast<int2*>(P.ws.seq) + b, make_int2(0, 0));
+    if (threadIdx.x == 0) {
+      __stcg(reinterpret_cast<int4*>(P.ws.seq + b), make_int4(0, 0, 0, 0));
+      __stcg(reinterpret_cast<int4*>(P.ws.seq + b) + 1, make_int4(0, 0, 0, 0));
+    }
   }
   if (threadIdx.x >= 32) return;
   int32_t* out = P.out_tokens + (size_t)b * P.out_w;
