@@ -919,9 +919,10 @@ __global__ void __launch_bounds__(kRingThreads, kRingMinCtas) row_pass_ring(cons
 // samples with top-p 0.8): every target and draft row of a sequence goes
 // through the same filter before the rule.  Order: temperature, top-k, then
 // top-p on the top-k distribution.  Both are value thresholds, so ties at a
-// threshold are kept.  One cluster of CTAs per row (each CTA scans one
-// segment of the row; their histograms are summed at the cluster's first CTA
-// through distributed shared memory) finds each threshold in two steps:
+// threshold are kept.  One CTA per row -- or a cluster of CTAs, each scanning
+// one segment of the row, their histograms summed at the cluster's first CTA
+// through distributed shared memory (filter_cluster_ctas says when) -- finds
+// each threshold in two steps:
 //   1. histograms of count and mass exp((x - m) / T) by distance below the row
 //      max (m from the row pass) pick the bin where the count (top-k) or the
 //      mass (top-p) summed from the top first reaches its target.  The bins
