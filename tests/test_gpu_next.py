@@ -223,6 +223,16 @@ def test_filtered_fp32_c1(sv):
         _filtered(sv, w, 77 + s, 0, 0.6)
 
 
+@pytest.mark.parametrize("V", [1, 2, 7, 1001, 8193])
+@pytest.mark.parametrize("dtype", [wl.BF16, wl.FP32])
+def test_filtered_ragged_vocabularies(sv, V, dtype):
+    """Rows with no full batch of 16-byte vectors (every id takes the per-id
+    test) and rows with a ragged tail, through top-k, top-p and both."""
+    w = wl.gaussian_pair(4, 3, V, dtype, 0.9, seed=V + 7, sigma_t=2.0, sigma_d=1.0)
+    for top_k, top_p in [(3, 0.0), (0, 0.7), (2, 0.5), (1, 0.0)]:
+        _filtered(sv, w, 300 + V, top_k, top_p)
+
+
 def test_filtered_ties_and_masked_vocabulary(sv):
     rng = np.random.default_rng(12)
     B, k, V = 6, 4, 3000
