@@ -291,6 +291,22 @@ def test_filtered_rows_cut_across_a_cluster(sv, dtype, V, ties):
     assert cut == (0 if V * esize < 131072 else 4)
 
 
+@pytest.mark.parametrize("top_k,top_p", [(0, 0.8), (20, 0.9)])
+def test_filtered_with_lenience_and_sequence_offset(sv, top_k, top_p):
+    """Filtering, asymmetric lenience and a shard's sequence offset in one call:
+    the rule on the filtered rows with l = 2, drawing the randomness of
+    sequences 100.. of a larger batch."""
+    for s_ in range(3):
+        w = wl.c2(seed=900 + s_)
+        t, d, x = to_device(w.target, w.dtype), to_device(w.draft, w.dtype), tokens_to_device(w.tokens)
+        out, n, aux = sv.verify_ex(t, d, x, w.temperature, 55 + s_, aux=True, top_k=top_k, top_p=top_p, lenience=2.0,
+                                   sequence_offset=100)
+        torch.cuda.synchronize()
+        ref = ox.verify_filtered(w.target, w.draft, w.tokens, w.dtype, w.temperature, 55 + s_, top_k, top_p,
+                                 seq_offset=100, lenience=2.0)
+        TALLY.add(compare_stochastic(ref, out.cpu().numpy(), n.cpu().numpy(), aux["status"].cpu().numpy(), w.k))
+
+
 def test_filtering_is_ignored_in_greedy_mode(sv):
     w = wl.c4(0.8, seed=3, B=4, k=6, V=2000)
     t, x = to_device(w.target, w.dtype), tokens_to_device(w.tokens)
