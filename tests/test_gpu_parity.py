@@ -80,6 +80,16 @@ def test_c3_headline_stochastic_and_greedy(sv):
     run_greedy(sv, w)
 
 
+@pytest.mark.parametrize("T", [0.3, 1.5])
+def test_c3_shape_at_other_temperatures(sv, T):
+    """C3's rows (Zipf-biased N(0, 4^2), V = 128256, bf16, k = 8) at a peaked and
+    a flat temperature, 16 sequences: the draw's floors and bound pruning
+    across very different candidate counts."""
+    w = wl.gaussian_pair(16, 8, 128256, wl.BF16, T, seed=int(T * 1000), sigma_t=4.0, sigma_d=1.0, zipf_s=1.1)
+    for vs in range(2):
+        run_stochastic(sv, w, seed=4321 + vs)
+
+
 @pytest.mark.parametrize("a", [0.6, 0.8])
 def test_c4_phrase_drafts_greedy(sv, a):
     """B=16, k=16, V=64000: bit-exact, and the committed count follows (1-a^17)/(1-a)."""
